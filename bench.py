@@ -1,0 +1,467 @@
+"""Benchmark of the absorbed-MLA hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole path over one batch of the workload:
+absorb (wk_b into the query) -> causal latent attention -> late
+decompression (wv_b); decode workloads add the split-KV combine and q8_0
+workloads dequantise the cache inside the attention kernel.  Inputs are the
+seeded synthetic tensors of ``workloads.py`` (no dataset), resident in HBM
+when the timed region starts.  L2 (129 MB) is flushed by writing a 512 MB
+buffer before every timed step; only the step itself is inside the CUDA events.
+
+``--impl reference`` times the CPU oracle (the un-absorbed definition in
+numpy fp64) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_latent_kv_lat_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA attn TFLOP/s (prefill) & HBM GB/s (decode) on 1 GB300, % of roofline"
+DEFAULT_WORKLOAD = "lite_t4096"
+DECODE_WORKLOAD = "v3_decode_b32"
+FLOP_PER_PAIR_HEAD = 2 * 576 + 2 * 512          # scores (576-d) + latent weighted sum (512-d)
+KERNEL_SOURCES = ["attn_simt.cu", "misc.cu", "api.cu", "kernels.cuh", "common.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+def attn_flops(wl: W.Workload, x: W.Inputs) -> float:
+    if wl.kind == "prefill":
+        pairs = wl.T * wl.q_pos0 + wl.T * (wl.T + 1) // 2
+    else:
+        pairs = int(x.seq_len.astype(np.int64).sum())
+    return float(pairs) * wl.n_head * FLOP_PER_PAIR_HEAD
+
+
+def decode_bytes(wl: W.Workload, x: W.Inputs) -> float:
+    row = 576 * 2 if wl.cache == "bf16" else 576 + 18 * 2
+    q = wl.B * wl.n_head * (512 + 64) * 2
+    o = wl.B * wl.n_head * 512 * 2
+    return float(x.seq_len.astype(np.int64).sum()) * row + q + o
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        p = os.path.join(ROOT, "mla_latent_kv_lat_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(p)).get(f"{kernel}:{workload}")
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def setup_workload(name, torch):
+    import mla_latent_kv_lat_gb300 as mla
+    from mla_latent_kv_lat_gb300 import pipeline as P
+    wl = W.WORKLOADS[name]
+    x = W.make_inputs(wl)
+
+    def dev(a):
+        return torch.from_numpy(W.to_bf16(a)[1]).view(torch.bfloat16).cuda()
+
+    d = {"q_nope": dev(x.q_nope), "q_pe": dev(x.q_pe), "wk_b": dev(x.wk_b), "wv_b": dev(x.wv_b)}
+    kv = torch.from_numpy(x.kv_rows_bits()).view(torch.bfloat16).cuda()
+    if wl.cache == "q8_0":
+        n = kv.shape[0]
+        d["kv_q"] = torch.empty(n, 576, dtype=torch.int8, device="cuda")
+        d["kv_d"] = torch.empty(18, n, dtype=torch.float16, device="cuda")
+        mla.mla_quantize_q8_0(kv, d["kv_q"], d["kv_d"])         # the cache producer, outside the timing
+        del kv
+    else:
+        d["kv"] = kv
+    if wl.kind == "decode":
+        d["seq_start"] = torch.from_numpy(x.seq_start).cuda()
+        d["seq_len"] = torch.from_numpy(x.seq_len).cuda()
+        max_len = int(x.seq_len.max())
+        bufs = P.decode_buffers(wl.B, wl.n_head, max_len)
+
+        def step(stream=None, ev=None):
+            mla.mla_absorb_q(d["q_nope"], d["wk_b"], bufs.q_lat, stream=stream)
+            if ev:
+                ev[0].record()
+            if wl.cache == "q8_0":
+                mla.mla_attn_decode_q8_0(bufs.q_lat, d["q_pe"], d["kv_q"], d["kv_d"], d["seq_start"], d["seq_len"],
+                                         max_len, bufs.workspace, bufs.o_lat, stream=stream)
+            else:
+                mla.mla_attn_decode(bufs.q_lat, d["q_pe"], d["kv"], d["seq_start"], d["seq_len"], max_len,
+                                    bufs.workspace, bufs.o_lat, stream=stream)
+            if ev:
+                ev[1].record()
+            mla.mla_late_decompress(bufs.o_lat, d["wv_b"], bufs.o, stream=stream)
+        launches = 4
+    else:
+        bufs = P.prefill_buffers(wl.T, wl.n_head)
+
+        def step(stream=None, ev=None):
+            mla.mla_absorb_q(d["q_nope"], d["wk_b"], bufs.q_lat, stream=stream)
+            if ev:
+                ev[0].record()
+            if wl.cache == "q8_0":
+                mla.mla_attn_prefill_q8_0(bufs.q_lat, d["q_pe"], d["kv_q"], d["kv_d"], wl.q_pos0, bufs.o_lat,
+                                          stream=stream)
+            else:
+                mla.mla_attn_prefill(bufs.q_lat, d["q_pe"], d["kv"], wl.q_pos0, bufs.o_lat, stream=stream)
+            if ev:
+                ev[1].record()
+            mla.mla_late_decompress(bufs.o_lat, d["wv_b"], bufs.o, stream=stream)
+        launches = 3
+    return wl, x, d, bufs, step, launches
+
+
+def time_steps(torch, step, steps, warmup, flush):
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    step_ms, attn_ms = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step(ev=(a0, a1))
+        e1.record()
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        attn_ms.append(a0.elapsed_time(a1))
+    return step_ms, attn_ms
+
+
+def run_ours(args, torch, dist, rank, world):
+    import mla_latent_kv_lat_gb300 as mla
+    from mla_latent_kv_lat_gb300 import build
+    if rank == 0 or not os.path.exists(build.LIB):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    mla.load_library()
+    pk, pk_kind = peaks()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+
+    wl, x, d, bufs, step, launches = setup_workload(args.workload, torch)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_wall = time.perf_counter()
+        step_ms, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+        t_wall = time.perf_counter() - t_wall
+    err = mla.mla_get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error {err} during the bench")
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    if wl.kind == "prefill":
+        units = attn_flops(wl, x)
+        value = units * world / (ms_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        ach = attn_flops(wl, x) / (attn_avg * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst"}
+    else:
+        units = decode_bytes(wl, x)
+        value = units * world / (ms_step * 1e-3) / 1e9
+        unit = "GB/s"
+        ach = decode_bytes(wl, x) / (attn_avg * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} HBM copy"}
+    kname = "attn_simt_kernel"
+    roof["traffic"] = recorded_traffic(kname, wl.name)
+    roof["kernel"] = kname
+    roof["attn_ms"] = round(attn_avg, 4)
+
+    out = {"metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.cache == "bf16" else "bf16+q8_0 cache",
+           "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan_in)) weights)",
+           "config": {"workload": wl.name, "describe": wl.describe, "n_head": wl.n_head, "cache": wl.cache,
+                      "T": wl.T, "q_pos0": wl.q_pos0, "n_kv": wl.n_kv, "B": wl.B,
+                      "parallelism": "replicas" if world > 1 else "single GPU",
+                      "l2": "flushed before every step (512 MB write)"},
+           "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clk.summary(),
+           "wall_s_timed": round(t_wall, 3)}
+    out["e2e"] = e2e_prefill(args, torch, wl, x, d, bufs) if wl.kind == "prefill" else e2e_decode(args, torch, wl, x, d,
+                                                                                                   bufs)
+    if args.with_decode and wl.kind == "prefill":
+        out["decode"] = secondary(args, torch, DECODE_WORKLOAD, flush, pk, pk_kind)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, x, unit, budget_s=args.cpu_budget)
+    return out
+
+
+def secondary(args, torch, name, flush, pk, pk_kind):
+    wl, x, d, bufs, step, launches = setup_workload(name, torch)
+    step_ms, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+    ms = sum(step_ms) / len(step_ms)
+    attn = sum(attn_ms) / len(attn_ms)
+    gbs = decode_bytes(wl, x) / (ms * 1e-3) / 1e9
+    ach = decode_bytes(wl, x) / (attn * 1e-3) / 1e9
+    return {"workload": name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(ach / pk["hbm_gbs"], 4), "peak_kind": f"{pk_kind} HBM copy",
+                         "attn_ms": round(attn, 4), "kernel": "attn_simt_kernel+combine_kernel"},
+            "tflops": round(attn_flops(wl, x) / (attn * 1e-3) / 1e12, 2)}
+
+
+def e2e_prefill(args, torch, wl, x, d, bufs):
+    """Same metric through the public pipeline with pinned host buffers: every
+    step copies its inputs host->device and the output o device->host."""
+    from mla_latent_kv_lat_gb300 import pipeline as P
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    out_host = torch.empty(bufs.o.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * 4
+    for _ in range(args.warmup):
+        P.mla_prefill_host(host, wl.q_pos0, d, bufs, out_host)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        P.mla_prefill_host(host, wl.q_pos0, d, bufs, out_host)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    return {"value": round(attn_flops(wl, x) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def e2e_decode(args, torch, wl, x, d, bufs):
+    import mla_latent_kv_lat_gb300 as mla
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    out_host = torch.empty(bufs.o.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    max_len = int(x.seq_len.max())
+
+    def one():
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        kw = dict(kv_q=d["kv_q"], kv_d=d["kv_d"]) if wl.cache == "q8_0" else dict(kv=d["kv"])
+        mla.mla_decode(d["q_nope"], d["q_pe"], d["wk_b"], d["wv_b"], d["seq_start"], d["seq_len"], max_len,
+                       bufs=bufs, **kw)
+        out_host.copy_(bufs.o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    return {"value": round(decode_bytes(wl, x) / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * 4}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(wl: W.Workload, x: W.Inputs, rows: int):
+    """Run the oracle (un-absorbed definition) on the first `rows` query rows
+    (prefill) or sequences (decode); returns (seconds, units done)."""
+    from oracle import mla_oracle as O
+    t0 = time.perf_counter()
+    if wl.kind == "prefill":
+        c_kv, k_pe = x.c_kv, x.k_pe
+        if wl.cache == "q8_0":
+            codes, scales = O.quantize_q8_0(np.concatenate([c_kv, k_pe], axis=1))
+            deq = O.dequantize_q8_0(codes, scales)
+            c_kv, k_pe = deq[:, :512], deq[:, 512:]
+            t0 = time.perf_counter()
+        sel = np.arange(wl.T - rows, wl.T)          # the last rows see the most keys
+        O.attention_unabsorbed(x.q_nope[sel], x.q_pe[sel], c_kv, k_pe, x.wk_b, x.wv_b, x.q_pos()[sel], wl.scale)
+        pairs = int((x.q_pos()[sel] + 1).sum())
+        units = pairs * wl.n_head * FLOP_PER_PAIR_HEAD
+    else:
+        seqs = list(range(rows))
+        O.decode_unabsorbed(x.q_nope, x.q_pe, x.c_kv, x.k_pe, x.wk_b, x.wv_b, x.seq_start, x.seq_len, wl.scale,
+                            seqs=seqs)
+        row = 576 * 2 if wl.cache == "bf16" else 612
+        units = int(x.seq_len[seqs].astype(np.int64).sum()) * row + len(seqs) * wl.n_head * (576 + 512) * 2
+    return time.perf_counter() - t0, units
+
+
+def cpu_baseline(wl, x, unit, budget_s=20.0):
+    rows = 4 if wl.kind == "prefill" else 1
+    sec, units = oracle_sample(wl, x, rows)
+    # grow the sample toward the time budget, then report the largest
+    while sec < budget_s / 4 and rows < (wl.T if wl.kind == "prefill" else wl.B):
+        rows = min(rows * 4, wl.T if wl.kind == "prefill" else wl.B)
+        sec, units = oracle_sample(wl, x, rows)
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    what = f"last {rows} query rows (all heads)" if wl.kind == "prefill" else f"first {rows} sequences"
+    return {"value": units / sec / scale, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{what} of {wl.name}, un-absorbed numpy fp64 oracle, {sec:.2f} s"}
+
+
+def run_reference(args):
+    wl = W.WORKLOADS[args.workload]
+    x = W.make_inputs(wl)
+    unit = "TFLOP/s" if wl.kind == "prefill" else "GB/s"
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    rows = 32 if wl.kind == "prefill" else 1
+    for _ in range(args.warmup):
+        oracle_sample(wl, x, rows)
+    tot_s = tot_u = 0.0
+    for _ in range(args.steps):
+        s, u = oracle_sample(wl, x, rows)
+        tot_s += s
+        tot_u += u
+    value = tot_u / tot_s / scale
+    what = f"last {rows} query rows" if wl.kind == "prefill" else f"first {rows} sequence"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "describe": wl.describe},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{what} of {wl.name} per step"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-decode", dest="with_decode", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    out = run_ours(args, torch, dist, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention computed directly on
+ * the compressed latent KV cache by matrix absorption, on one NVIDIA GB300
+ * (sm_103a).
+ *
+ * The method is the one described on the page "MLA matrix absorption in
+ * ik_llama.cpp" (czykbl.com/news/93068):
+ *   sec. 3  K absorption: the K up-projection is folded into the query,
+ *           q_lat[h] = wk_b[h]^T q_nope[h]                       (128 -> 512)
+ *   sec. 5  move elision: scores are split into a RoPE part and a latent
+ *           part, s = q_pe . k_pe + q_lat . c_kv, with no concatenation
+ *   sec. 8.1 FlashMLA: causal online softmax over the latent cache
+ *   sec. 4  V absorption: the weighted sum stays in latent space,
+ *           o_lat = P c_kv, and W^UV is applied late, o[h] = wv_b[h] o_lat[h]
+ *   sec. 8.1 MLA with a Q8_0-quantised latent cache.
+ * Dimensions follow the DeepSeek GGUF metadata quoted on the page
+ * "ik_llama.cpp PR #394 mainline DeepSeek GGUF support" (czykbl.com/news/94940),
+ * sec. 2.1: kv_lora_rank 512, rope 64, nope 128, v 128, key_length 576.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked "device" are device memory of the current CUDA device,
+ *   allocated, owned and freed by the caller.  No entry point allocates
+ *   device or host memory, and none keeps a pointer after it returns.
+ * - bf16 buffers are raw bfloat16 bit patterns (uint16_t); fp16 likewise.
+ * - Every device pointer must be 16-byte aligned (MLA_ERR_MISALIGNED).
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Work is enqueued asynchronously on it; host arguments are
+ *   validated before anything is enqueued, and a validation error returns
+ *   at once with nothing launched.
+ * - Return value: MLA_OK or a negative mla_status.  Nothing aborts, traps or
+ *   prints.  A launch error reported by the CUDA runtime maps to MLA_ERR_CUDA.
+ * - Kernels that wait on asynchronous copies or tensor-core work bound every
+ *   wait.  A wait that runs out records MLA_ERR_TIMEOUT in a per-device error
+ *   word, abandons its tile and returns; mla_get_device_error() reads it.
+ * - Dims other than kv_lora_rank 512, qk_rope 64, qk_nope 128, v_head 128,
+ *   or n_head not a multiple of 16 in [16, 128], return MLA_ERR_UNSUPPORTED.
+ *
+ * Cache layouts
+ * -------------
+ * bf16 latent cache `kv`: row-major [n_rows][576] bf16.  Columns 0..511 hold
+ *   c_kv (the latent), 512..575 hold k_pe (the RoPE key, shared by all
+ *   heads): 1152 bytes per cached token, the "1.15 KB" of the method page,
+ *   sec. 7.  Row j of a prefill cache holds position j.
+ * q8_0 latent cache: the same 576 values per row, quantised in 18 blocks of
+ *   32 (the Q8_0 cache of sec. 8.1; 18 x 34 = 612 bytes per row):
+ *     kv_q  int8 [n_rows][576]   codes, row-major;
+ *     kv_d  fp16 [18][n_rows]    block scales, block-major (scale of row j,
+ *                                block b at kv_d[b * n_rows + j]).
+ *   Element i of block b of row j is x = kv_d[b][j] * kv_q[j][32 b + i].
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mla_dims {
+  int32_t n_head;        /* H: heads; a multiple of 16 in [16, 128]            */
+  int32_t kv_lora_rank;  /* must be 512 (latent width)                         */
+  int32_t qk_rope;       /* must be 64  (RoPE part of keys and queries)        */
+  int32_t qk_nope;       /* must be 128 (non-RoPE query part per head)         */
+  int32_t v_head;        /* must be 128 (value width per head)                 */
+  float scale;           /* softmax scale on q.k, e.g. 1/sqrt(128 + 64)        */
+} mla_dims;
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, bad positions */
+  MLA_ERR_UNSUPPORTED = -2,  /* dims outside the supported set                 */
+  MLA_ERR_MISALIGNED = -3,   /* a device pointer is not 16-byte aligned        */
+  MLA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required     */
+  MLA_ERR_CUDA = -5,         /* the CUDA runtime reported an error             */
+  MLA_ERR_TIMEOUT = -6       /* a device-side bounded wait ran out             */
+} mla_status;
+
+/* Step 1, K absorption (method page sec. 3 and the q_nope2 line of sec. 4):
+ *   q_lat[t][h][c] = sum_d q_nope[t][h][d] * wk_b[h][d][c]
+ * q_nope  device bf16 [T][H][128]
+ * wk_b    device bf16 [H][128][512]   (K up-projection, per head)
+ * q_lat   device bf16 [T][H][512]     output, fp32 accumulation, rounded once
+ * T >= 1.                                                                     */
+int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b,
+                 void* q_lat, int32_t T, void* stream);
+
+/* Steps 2-4 for a causal prefill chunk (method page sec. 4, 5, 8.1):
+ *   s[t][h][j] = scale * (q_pe[t][h] . k_pe[j] + q_lat[t][h] . c_kv[j])
+ *   visible iff j <= q_pos0 + t   (query t sits at position q_pos0 + t)
+ *   o_lat[t][h] = sum_j softmax_j(s[t][h]) * c_kv[j]
+ * q_lat   device bf16 [T][H][512]
+ * q_pe    device bf16 [T][H][64]
+ * kv      device bf16 [n_kv][576]    latent cache (layout above)
+ * o_lat   device bf16 [T][H][512]    output
+ * lse     device fp32 [T][H] or NULL; natural-log sum_j exp(s[t][h][j])
+ * Requires T >= 1, q_pos0 >= 0 and q_pos0 + T <= n_kv.  Rows past
+ * q_pos0 + T - 1 are never read.                                              */
+int mla_attn_prefill(const mla_dims* dims, const void* q_lat, const void* q_pe,
+                     const void* kv, int32_t n_kv, int32_t T, int32_t q_pos0,
+                     void* o_lat, float* lse, void* stream);
+
+/* As mla_attn_prefill over a q8_0 latent cache (method page sec. 8.1):
+ * kv_q device int8 [n_kv][576], kv_d device fp16 [18][n_kv].  Each block is
+ * dequantised as fp16 scale x int8 code before it enters the scores and the
+ * latent weighted sum.                                                        */
+int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe,
+                          const int8_t* kv_q, const uint16_t* kv_d, int32_t n_kv,
+                          int32_t T, int32_t q_pos0, void* o_lat, float* lse,
+                          void* stream);
+
+/* Bytes of device workspace mla_attn_decode / mla_attn_decode_q8_0 need for
+ * B sequences no longer than max_len (split-KV partial results).  Returns 0
+ * for invalid arguments.  The value depends only on the arguments and the
+ * current device.                                                             */
+size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_len);
+
+/* Steps 2-4 for one new token per sequence (decode), with split-KV and a
+ * log-sum-exp combine of the partial results:
+ *   sequence b's cache rows are kv[seq_start[b] .. seq_start[b] + seq_len[b]),
+ *   its query sits at position seq_len[b] - 1 and sees all of them.
+ * q_lat      device bf16 [B][H][512];  q_pe device bf16 [B][H][64]
+ * kv         device bf16 [n_rows][576] (rows of all sequences)
+ * seq_start  device int64 [B]  first row of each sequence
+ * seq_len    device int32 [B]  1 <= seq_len[b] <= max_len, rows inside kv
+ * workspace  device, ws_bytes >= mla_decode_workspace_size(dims, B, max_len)
+ * o_lat      device bf16 [B][H][512]  output
+ * n_rows is the row count of kv (used for argument checks and the q8_0
+ * scale layout).  seq_start/seq_len are read on the device only.              */
+int mla_attn_decode(const mla_dims* dims, const void* q_lat, const void* q_pe,
+                    const void* kv, int64_t n_rows, const int64_t* seq_start,
+                    const int32_t* seq_len, int32_t B, int32_t max_len,
+                    void* workspace, size_t ws_bytes, void* o_lat, void* stream);
+
+/* As mla_attn_decode over a q8_0 cache: kv_q int8 [n_rows][576], kv_d fp16
+ * [18][n_rows].                                                               */
+int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe,
+                         const int8_t* kv_q, const uint16_t* kv_d, int64_t n_rows,
+                         const int64_t* seq_start, const int32_t* seq_len, int32_t B,
+                         int32_t max_len, void* workspace, size_t ws_bytes,
+                         void* o_lat, void* stream);
+
+/* Step 5, late decompression (method page sec. 4, the wv_b line):
+ *   o[t][h][e] = sum_c o_lat[t][h][c] * wv_b[h][c][e]
+ * o_lat device bf16 [T][H][512]; wv_b device bf16 [H][512][128];
+ * o     device fp32 [T][H][128] output.  T >= 1.                              */
+int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b,
+                        float* o, int32_t T, void* stream);
+
+/* Quantise n bf16 cache rows [n][576] to the q8_0 layout above (the producer
+ * of the sec. 8.1 cache).  Per block: amax = max |x|, d = amax / 127 (fp32),
+ * q = round-half-away-from-zero(x / d) clamped to [-127, 127] (0 when
+ * amax = 0), stored scale fp16(d).  kv_d is [18][ld_d] with ld_d >= n: row
+ * j's scales go to kv_d[b * ld_d + j].                                        */
+int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n,
+                      int64_t ld_d, void* stream);
+
+/* Synchronise `stream`, then return and clear the current device's error
+ * word: MLA_OK, or the first device-side error (MLA_ERR_TIMEOUT) recorded
+ * since the last call.  MLA_ERR_CUDA if the synchronisation itself fails.     */
+int mla_get_device_error(void* stream);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier phase nothing completes, giving up after `spins` polls (1 <= spins
+ * <= 1<<20).  It records MLA_ERR_TIMEOUT in the device error word exactly as
+ * a kernel's real waits do, and returns normally.  No counterpart on the
+ * pages: it exists so that tests can check failure reporting without
+ * hanging or faulting a GPU.                                                  */
+int mla_selftest_wait_timeout(int32_t spins, void* stream);
+
+/* Static description of a status code (never NULL).                           */
+const char* mla_status_string(int status);
+
+/* Library version string, e.g. "mla-gb300 0.1 sm_103a".                      */
+const char* mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,262 @@
+// The C ABI of libmla (declared in include/mla.h): argument validation,
+// launch planning and the per-device error word.  Every step of the path runs
+// in the kernels launched from here; there is no host or fallback compute.
+#include <stdint.h>
+
+#include "kernels.cuh"
+
+namespace mla {
+namespace {
+
+__device__ int g_device_error;   // first device-side error since the last read
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+
+// Device address of the current device's error word (set up once per device).
+cudaError_t error_word(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const mla_dims* d) {
+  if (d == nullptr) return MLA_ERR_INVALID_ARG;
+  if (d->kv_lora_rank != kLatent || d->qk_rope != kRope || d->qk_nope != kNope || d->v_head != kVHead)
+    return MLA_ERR_UNSUPPORTED;
+  if (d->n_head < 16 || d->n_head > 128 || d->n_head % 16 != 0) return MLA_ERR_UNSUPPORTED;
+  if (!(d->scale > 0.f) || !(d->scale < 1e30f)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (p == nullptr) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MLA_ERR_MISALIGNED;
+  }
+  return MLA_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+// Split-KV plan of the decode kernels: keys per split and splits per sequence.
+struct DecodePlan {
+  int chunk;
+  int n_split;
+};
+
+DecodePlan decode_plan(int32_t max_len) {
+  DecodePlan p;
+  p.chunk = 2048;
+  p.n_split = static_cast<int>((static_cast<int64_t>(max_len) + p.chunk - 1) / p.chunk);
+  return p;
+}
+
+size_t decode_ws_bytes(int H, int32_t B, int32_t max_len) {
+  const DecodePlan p = decode_plan(max_len);
+  const size_t slots = static_cast<size_t>(B) * p.n_split * H;
+  return slots * kLatent * sizeof(float) + slots * 2 * sizeof(float);
+}
+
+int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv,
+                   const int8_t* kv_q, const uint16_t* kv_d, int32_t n_kv, int32_t T, int32_t q_pos0,
+                   void* o_lat, float* lse, void* stream, bool q8) {
+  int s = check_dims(dims);
+  if (s != MLA_OK) return s;
+  s = q8 ? check_ptrs({q_lat, q_pe, kv_q, kv_d, o_lat}) : check_ptrs({q_lat, q_pe, kv, o_lat});
+  if (s != MLA_OK) return s;
+  if (lse != nullptr && !aligned16(lse)) return MLA_ERR_MISALIGNED;
+  if (T < 1 || q_pos0 < 0 || n_kv < 1) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(q_pos0) + T > n_kv) return MLA_ERR_INVALID_ARG;
+  int* err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  AttnArgs a = {};
+  a.q_lat = q_lat;
+  a.q_pe = q_pe;
+  a.kv = kv;
+  a.kv_q = kv_q;
+  a.kv_d = kv_d;
+  a.ld_d = n_kv;
+  a.n_head = dims->n_head;
+  a.scale = dims->scale;
+  a.q_pos0 = q_pos0;
+  a.o_lat = o_lat;
+  a.lse = lse;
+  a.decode = 0;
+  a.err = err;
+  a.wait_polls = kDefaultWaitPolls;
+  return to_status(launch_attn_simt(a, q8, T, static_cast<cudaStream_t>(stream)));
+}
+
+int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, const int8_t* kv_q,
+                  const uint16_t* kv_d, int64_t n_rows, const int64_t* seq_start, const int32_t* seq_len,
+                  int32_t B, int32_t max_len, void* workspace, size_t ws_bytes, void* o_lat, void* stream,
+                  bool q8) {
+  int s = check_dims(dims);
+  if (s != MLA_OK) return s;
+  s = q8 ? check_ptrs({q_lat, q_pe, kv_q, kv_d, o_lat}) : check_ptrs({q_lat, q_pe, kv, o_lat});
+  if (s != MLA_OK) return s;
+  if (seq_start == nullptr || seq_len == nullptr) return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seq_start) & 7u) || (reinterpret_cast<uintptr_t>(seq_len) & 3u))
+    return MLA_ERR_MISALIGNED;
+  if (B < 1 || max_len < 1 || n_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (B > 65535) return MLA_ERR_UNSUPPORTED;
+  const size_t need = decode_ws_bytes(dims->n_head, B, max_len);
+  if (workspace == nullptr || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_MISALIGNED;
+  int* err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  const DecodePlan plan = decode_plan(max_len);
+  const size_t slots = static_cast<size_t>(B) * plan.n_split * dims->n_head;
+  AttnArgs a = {};
+  a.q_lat = q_lat;
+  a.q_pe = q_pe;
+  a.kv = kv;
+  a.kv_q = kv_q;
+  a.kv_d = kv_d;
+  a.ld_d = n_rows;
+  a.n_head = dims->n_head;
+  a.scale = dims->scale;
+  a.decode = 1;
+  a.seq_start = seq_start;
+  a.seq_len = seq_len;
+  a.n_split = plan.n_split;
+  a.chunk = plan.chunk;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = a.ws_o + slots * kLatent;
+  a.err = err;
+  a.wait_polls = kDefaultWaitPolls;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = launch_attn_simt(a, q8, B * plan.n_split, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  CombineArgs c = {};
+  c.ws_o = a.ws_o;
+  c.ws_ml = a.ws_ml;
+  c.seq_len = seq_len;
+  c.o_lat = o_lat;
+  c.B = B;
+  c.n_head = dims->n_head;
+  c.n_split = plan.n_split;
+  c.chunk = plan.chunk;
+  return to_status(launch_combine(c, st));
+}
+
+int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32_t T, int K, int N, bool f32,
+              void* stream) {
+  int s = check_dims(dims);
+  if (s != MLA_OK) return s;
+  s = check_ptrs({a, w, c});
+  if (s != MLA_OK) return s;
+  if (T < 1) return MLA_ERR_INVALID_ARG;
+  if ((T + 63) / 64 > 65535) return MLA_ERR_UNSUPPORTED;
+  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0};
+  return to_status(launch_head_gemm_simt(g, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b, void* q_lat, int32_t T,
+                 void* stream) {
+  return head_gemm(dims, q_nope, wk_b, q_lat, T, kNope, kLatent, false, stream);
+}
+
+int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b, float* o, int32_t T,
+                        void* stream) {
+  return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, true, stream);
+}
+
+int mla_attn_prefill(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, int32_t n_kv,
+                     int32_t T, int32_t q_pos0, void* o_lat, float* lse, void* stream) {
+  return prefill_common(dims, q_lat, q_pe, kv, nullptr, nullptr, n_kv, T, q_pos0, o_lat, lse, stream, false);
+}
+
+int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe, const int8_t* kv_q,
+                          const uint16_t* kv_d, int32_t n_kv, int32_t T, int32_t q_pos0, void* o_lat,
+                          float* lse, void* stream) {
+  return prefill_common(dims, q_lat, q_pe, nullptr, kv_q, kv_d, n_kv, T, q_pos0, o_lat, lse, stream, true);
+}
+
+size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_len) {
+  if (check_dims(dims) != MLA_OK || B < 1 || max_len < 1) return 0;
+  return decode_ws_bytes(dims->n_head, B, max_len);
+}
+
+int mla_attn_decode(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, int64_t n_rows,
+                    const int64_t* seq_start, const int32_t* seq_len, int32_t B, int32_t max_len, void* workspace,
+                    size_t ws_bytes, void* o_lat, void* stream) {
+  return decode_common(dims, q_lat, q_pe, kv, nullptr, nullptr, n_rows, seq_start, seq_len, B, max_len, workspace,
+                       ws_bytes, o_lat, stream, false);
+}
+
+int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe, const int8_t* kv_q,
+                         const uint16_t* kv_d, int64_t n_rows, const int64_t* seq_start, const int32_t* seq_len,
+                         int32_t B, int32_t max_len, void* workspace, size_t ws_bytes, void* o_lat, void* stream) {
+  return decode_common(dims, q_lat, q_pe, nullptr, kv_q, kv_d, n_rows, seq_start, seq_len, B, max_len, workspace,
+                       ws_bytes, o_lat, stream, true);
+}
+
+int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d, void* stream) {
+  int s = check_ptrs({kv, kv_q});
+  if (s != MLA_OK) return s;
+  if (kv_d == nullptr) return MLA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(kv_d) & 1u) return MLA_ERR_MISALIGNED;
+  if (n < 1 || ld_d < n) return MLA_ERR_INVALID_ARG;
+  if ((n * kQ8Blocks + 7) / 8 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  return to_status(launch_quantize_q8_0(kv, kv_q, kv_d, n, ld_d, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  int* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return v;
+}
+
+int mla_selftest_wait_timeout(int32_t spins, void* stream) {
+  if (spins < 1 || spins > (1 << 20)) return MLA_ERR_INVALID_ARG;
+  int* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
+  return to_status(launch_wait_timeout_selftest(static_cast<uint32_t>(spins), err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported dims or size";
+    case MLA_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* mla_version(void) { return "mla-gb300 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Internal kernel interfaces of libmla (not part of the C ABI).
+#pragma once
+
+#include "common.cuh"
+
+namespace mla {
+
+// Arguments of one latent-attention launch (prefill or decode partials).
+struct AttnArgs {
+  const void* q_lat;        // bf16 [rows][H][512]
+  const void* q_pe;         // bf16 [rows][H][64]
+  const void* kv;           // bf16 [n_rows][576]            (bf16 cache)
+  const int8_t* kv_q;       // int8 [n_rows][576]            (q8_0 cache)
+  const uint16_t* kv_d;     // fp16 [18][ld_d]               (q8_0 cache)
+  int64_t ld_d;
+  int n_head;
+  float scale;
+  // prefill
+  int q_pos0;
+  void* o_lat;              // bf16 [T][H][512]
+  float* lse;               // fp32 [T][H] or null
+  // decode
+  int decode;
+  const int64_t* seq_start;
+  const int32_t* seq_len;
+  int n_split;              // splits per sequence
+  int chunk;                // keys per split
+  float* ws_o;              // fp32 [B][n_split][H][512] unnormalised partial sums
+  float* ws_ml;             // fp32 [B][n_split][H][2]   running max (log2 units), sum
+  int* err;                 // device error word
+  uint32_t wait_polls;
+};
+
+struct CombineArgs {
+  const float* ws_o;
+  const float* ws_ml;
+  const int32_t* seq_len;
+  void* o_lat;
+  int B, n_head, n_split, chunk;
+};
+
+// C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: K=128, N=512, bf16 out;
+// late decompression: K=512, N=128, fp32 out).
+struct HeadGemmArgs {
+  const void* a;            // bf16 [T][H][K]
+  const void* w;            // bf16 [H][K][N]
+  void* c;                  // bf16 or fp32 [T][H][N]
+  int T, H, K, N;
+  int out_f32;
+};
+
+cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStream_t stream);
+size_t attn_simt_smem_bytes();
+cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
+cudaError_t launch_head_gemm_simt(const HeadGemmArgs& g, cudaStream_t stream);
+cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d,
+                                 cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,97 @@
+"""The whole absorbed-MLA hot path as one call per use case.
+
+Prefill: absorb (wk_b into the query) -> causal latent attention -> late
+decompression (wv_b).  Decode: the same with split-KV attention.  Each step is
+one C-ABI call of libmla on the caller's stream; this module only allocates
+the intermediate device buffers through PyTorch and, for the host variants,
+moves inputs and outputs between pinned host memory and the device.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+@dataclass
+class PrefillBuffers:
+    q_lat: torch.Tensor      # bf16 [T, H, 512]
+    o_lat: torch.Tensor      # bf16 [T, H, 512]
+    o: torch.Tensor          # fp32 [T, H, 128]
+    lse: Optional[torch.Tensor] = None
+
+
+def prefill_buffers(T: int, H: int, device="cuda", with_lse=False) -> PrefillBuffers:
+    return PrefillBuffers(
+        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(T, H, B.V_HEAD, dtype=torch.float32, device=device),
+        torch.empty(T, H, dtype=torch.float32, device=device) if with_lse else None)
+
+
+def mla_prefill(q_nope, q_pe, wk_b, wv_b, q_pos0: int, *, kv=None, kv_q=None, kv_d=None,
+                bufs: Optional[PrefillBuffers] = None, scale=None, stream=None) -> PrefillBuffers:
+    """o = late_decompress(attn(absorb(q_nope), q_pe, cache)) on device tensors.
+
+    Pass ``kv`` (bf16 [n_kv, 576]) or ``kv_q``/``kv_d`` (q8_0 cache)."""
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    if bufs is None:
+        bufs = prefill_buffers(T, H, q_nope.device)
+    B.mla_absorb_q(q_nope, wk_b, bufs.q_lat, scale=scale, stream=stream)
+    if kv is not None:
+        B.mla_attn_prefill(bufs.q_lat, q_pe, kv, q_pos0, bufs.o_lat, bufs.lse, scale=scale, stream=stream)
+    else:
+        B.mla_attn_prefill_q8_0(bufs.q_lat, q_pe, kv_q, kv_d, q_pos0, bufs.o_lat, bufs.lse, scale=scale,
+                                stream=stream)
+    B.mla_late_decompress(bufs.o_lat, wv_b, bufs.o, scale=scale, stream=stream)
+    return bufs
+
+
+@dataclass
+class DecodeBuffers:
+    q_lat: torch.Tensor
+    o_lat: torch.Tensor
+    o: torch.Tensor
+    workspace: torch.Tensor
+
+
+def decode_buffers(Bn: int, H: int, max_len: int, device="cuda") -> DecodeBuffers:
+    ws = B.mla_decode_workspace_size(H, Bn, max_len)
+    return DecodeBuffers(
+        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(Bn, H, B.V_HEAD, dtype=torch.float32, device=device),
+        torch.empty(ws, dtype=torch.uint8, device=device))
+
+
+def mla_decode(q_nope, q_pe, wk_b, wv_b, seq_start, seq_len, max_len: int, *, kv=None, kv_q=None, kv_d=None,
+               bufs: Optional[DecodeBuffers] = None, scale=None, stream=None) -> DecodeBuffers:
+    """One decode step for B sequences (one new token each) on device tensors."""
+    Bn, H = q_nope.shape[0], q_nope.shape[1]
+    if bufs is None:
+        bufs = decode_buffers(Bn, H, max_len, q_nope.device)
+    B.mla_absorb_q(q_nope, wk_b, bufs.q_lat, scale=scale, stream=stream)
+    if kv is not None:
+        B.mla_attn_decode(bufs.q_lat, q_pe, kv, seq_start, seq_len, max_len, bufs.workspace, bufs.o_lat,
+                          scale=scale, stream=stream)
+    else:
+        B.mla_attn_decode_q8_0(bufs.q_lat, q_pe, kv_q, kv_d, seq_start, seq_len, max_len, bufs.workspace,
+                               bufs.o_lat, scale=scale, stream=stream)
+    B.mla_late_decompress(bufs.o_lat, wv_b, bufs.o, scale=scale, stream=stream)
+    return bufs
+
+
+def mla_prefill_host(host: dict, q_pos0: int, dev: dict, bufs: PrefillBuffers, out_host: torch.Tensor,
+                     stream=None) -> torch.Tensor:
+    """Host-buffer prefill: copy each pinned host input into its device buffer,
+    run the path, copy o back into pinned ``out_host``.  ``host``/``dev`` map
+    input names (q_nope, q_pe, wk_b, wv_b and kv or kv_q/kv_d) to tensors."""
+    for k, t in host.items():
+        dev[k].copy_(t, non_blocking=True)
+    mla_prefill(dev["q_nope"], dev["q_pe"], dev["wk_b"], dev["wv_b"], q_pos0, kv=dev.get("kv"),
+                kv_q=dev.get("kv_q"), kv_d=dev.get("kv_d"), bufs=bufs, stream=stream)
+    out_host.copy_(bufs.o, non_blocking=True)
+    return out_host

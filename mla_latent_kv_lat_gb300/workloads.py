@@ -129,7 +129,8 @@ class Inputs:
         return to_bf16(np.concatenate([self.c_kv, self.k_pe], axis=1))[1]
 
 
-def _normal(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std) fp32 draws rounded to bf16 (values as float32)."""
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
@@ -178,12 +179,12 @@ def make_inputs(wl: Workload | str, seed: int = 0, *, n_head: Optional[int] = No
             raise ValueError("prefill queries must lie inside the cache")
         n_rows = wl.n_kv
         nq = wl.T
-    c_kv = _normal(rng, (n_rows, KV_LORA_RANK))
-    k_pe = _normal(rng, (n_rows, QK_ROPE))
-    q_nope = _normal(rng, (nq, H, QK_NOPE))
-    q_pe = _normal(rng, (nq, H, QK_ROPE))
-    wk_b = _normal(rng, (H, QK_NOPE, KV_LORA_RANK), 1.0 / math.sqrt(QK_NOPE))
-    wv_b = _normal(rng, (H, KV_LORA_RANK, V_HEAD), 1.0 / math.sqrt(KV_LORA_RANK))
+    c_kv = normal_bf16(rng, (n_rows, KV_LORA_RANK))
+    k_pe = normal_bf16(rng, (n_rows, QK_ROPE))
+    q_nope = normal_bf16(rng, (nq, H, QK_NOPE))
+    q_pe = normal_bf16(rng, (nq, H, QK_ROPE))
+    wk_b = normal_bf16(rng, (H, QK_NOPE, KV_LORA_RANK), 1.0 / math.sqrt(QK_NOPE))
+    wv_b = normal_bf16(rng, (H, KV_LORA_RANK, V_HEAD), 1.0 / math.sqrt(KV_LORA_RANK))
     return Inputs(wl, c_kv, k_pe, q_nope, q_pe, wk_b, wv_b, seq_len, seq_start)
 
 

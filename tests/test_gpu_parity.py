@@ -1,0 +1,278 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on seeded inputs.
+
+Tolerances are those of the stated target: max|d|/max|ref| <= 1e-2 and
+mean|d|/mean|ref| <= 2e-3 with a bf16 cache, 3e-2 / 5e-3 with a q8_0 cache.
+Small cases compare every output element; full-size workloads compare >= 512
+sampled query rows (always the first and the last, and rows at tile edges).
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_lat_gb300 as mla
+from mla_latent_kv_lat_gb300 import workloads as W
+from oracle import mla_oracle as O
+from tests.gpu_util import TOL_BF16, TOL_Q8, Dev, assert_tol, bf16_dev, dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from mla_latent_kv_lat_gb300 import build
+    build.build()
+    mla.load_library()
+    assert mla.mla_get_device_error() == 0
+
+
+def _check_no_device_error():
+    assert mla.mla_get_device_error() == 0
+
+
+def run_prefill(d: Dev, q_pos0, q8=False, lse=False):
+    x = d.x
+    bufs = mla.pipeline.prefill_buffers(x.q_nope.shape[0], x.wl.n_head, with_lse=lse)
+    if q8:
+        mla.mla_prefill(d.q_nope, d.q_pe, d.wk_b, d.wv_b, q_pos0, kv_q=d.kv_q, kv_d=d.kv_d, bufs=bufs)
+    else:
+        mla.mla_prefill(d.q_nope, d.q_pe, d.wk_b, d.wv_b, q_pos0, kv=d.kv, bufs=bufs)
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    return bufs
+
+
+def run_decode(d: Dev, q8=False):
+    x = d.x
+    max_len = int(x.seq_len.max())
+    kw = dict(kv_q=d.kv_q, kv_d=d.kv_d) if q8 else dict(kv=d.kv)
+    bufs = mla.mla_decode(d.q_nope, d.q_pe, d.wk_b, d.wv_b, d.seq_start, d.seq_len, max_len, **kw)
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    return bufs
+
+
+def sampled_rows(T, q_pos0, k=512, tile=128):
+    edges = [0, T - 1]
+    for t in range(0, T, max(1, T // 16)):
+        edges += [t, t + 1, t + tile - 1]
+    for t in range(T):
+        if (q_pos0 + t) % tile in (0, tile - 1) and len(edges) < 64:
+            edges.append(t)
+    return W.sample_rows(T, k, seed=0, must=tuple(edges))
+
+
+# ---------------------------------------------------------------------------
+# Single steps on seeded inputs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,T", [(16, 1), (16, 77), (16, 256), (128, 200), (48, 130)])
+def test_absorb_q_matches_oracle(H, T):
+    x = W.make_inputs("v3_chunk8192_at32768", n_head=H, T=T, q_pos0=0, n_kv=T)
+    q_nope, wk_b = bf16_dev(x.q_nope), bf16_dev(x.wk_b)
+    q_lat = torch.empty(T, H, 512, dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_q(q_nope, wk_b, q_lat)
+    got = dev_f32(q_lat)
+    ref = O.absorb_q(x.q_nope, x.wk_b)
+    # one bf16 rounding of an fp32 sum of 128 products
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * np.sqrt(np.mean(ref ** 2)))
+    _check_no_device_error()
+
+
+@pytest.mark.parametrize("H,T", [(16, 1), (16, 77), (128, 200), (32, 64)])
+def test_late_decompress_matches_oracle(H, T):
+    rng = np.random.default_rng(5)
+    o_lat = W.normal_bf16(rng, (T, H, 512), 0.3)
+    wv_b = W.normal_bf16(rng, (H, 512, 128), 1 / np.sqrt(512))
+    o = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
+    mla.mla_late_decompress(bf16_dev(o_lat), bf16_dev(wv_b), o)
+    got = o.cpu().numpy().astype(np.float64)
+    ref = O.late_decompress(o_lat, wv_b)
+    # fp32 accumulation of 512 bf16 x bf16 products (products exact in fp32)
+    assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(ref)) + 1e-6
+    _check_no_device_error()
+
+
+@pytest.mark.parametrize("H,T,q_pos0,n_kv", [(16, 256, 0, 256), (16, 100, 37, 200), (128, 33, 300, 333),
+                                            (16, 1, 0, 1), (64, 130, 0, 130)])
+def test_prefill_latent_attention_matches_oracle(H, T, q_pos0, n_kv):
+    x = W.make_inputs("lite_t256", n_head=H, T=T, q_pos0=q_pos0, n_kv=n_kv)
+    rng = np.random.default_rng(3)
+    q_lat = W.normal_bf16(rng, (T, H, 512))
+    d = Dev(x)
+    o_lat = torch.empty(T, H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    mla.mla_attn_prefill(bf16_dev(q_lat), d.q_pe, d.kv, q_pos0, o_lat, lse)
+    ref, ref_lse = O.attention_latent(q_lat, x.q_pe, x.c_kv, x.k_pe, x.q_pos(), x.wl.scale)
+    assert_tol(dev_f32(o_lat), ref, TOL_BF16, "o_lat")
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 2e-3
+    _check_no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# The whole path vs the un-absorbed definition
+# ---------------------------------------------------------------------------
+def test_prefill_chain_lite_t256_every_row():
+    x = W.make_inputs("lite_t256")
+    bufs = run_prefill(Dev(x), x.wl.q_pos0)
+    ref, _ = O.attention_unabsorbed(x.q_nope, x.q_pe, x.c_kv, x.k_pe, x.wk_b, x.wv_b, x.q_pos(), x.wl.scale)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_BF16, "lite_t256 o")
+
+
+def test_prefill_chain_lite_t4096_every_row():
+    x = W.make_inputs("lite_t4096")
+    bufs = run_prefill(Dev(x), x.wl.q_pos0)
+    ref, _ = O.attention_unabsorbed(x.q_nope, x.q_pe, x.c_kv, x.k_pe, x.wk_b, x.wv_b, x.q_pos(), x.wl.scale)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_BF16, "lite_t4096 o")
+
+
+def test_full_prefill_v3_chunk_sampled_rows():
+    x = W.make_inputs("v3_chunk8192_at32768")
+    bufs = run_prefill(Dev(x), x.wl.q_pos0)
+    rows = sampled_rows(x.wl.T, x.wl.q_pos0)
+    assert len(rows) >= 512
+    ref, _ = O.attention_unabsorbed(x.q_nope[rows], x.q_pe[rows], x.c_kv, x.k_pe, x.wk_b, x.wv_b,
+                                    x.q_pos()[rows], x.wl.scale)
+    assert_tol(bufs.o.cpu().numpy()[rows], ref, TOL_BF16, "v3 chunk o")
+
+
+def _decode_refs(x, c_kv, k_pe, n_heads_unabsorbed=4):
+    """Absorbed-form oracle for every head (pinned to the definition by the
+    associativity tests) plus the un-absorbed definition on sampled heads."""
+    q_lat = O.absorb_q(x.q_nope, x.wk_b)
+    o_lat, _ = O.decode_latent(q_lat, x.q_pe, c_kv, k_pe, x.seq_start, x.seq_len, x.wl.scale)
+    ref = O.late_decompress(o_lat, x.wv_b)
+    heads = list(W.sample_rows(x.wl.n_head, n_heads_unabsorbed, seed=1, must=(0, x.wl.n_head - 1)))
+    ref_u = O.decode_unabsorbed(x.q_nope, x.q_pe, c_kv, k_pe, x.wk_b, x.wv_b, x.seq_start, x.seq_len,
+                                x.wl.scale, heads=heads, seqs=[0, len(x.seq_len) - 1])
+    return ref, heads, ref_u
+
+
+def test_decode_chain_v3_b32_every_sequence():
+    x = W.make_inputs("v3_decode_b32")
+    bufs = run_decode(Dev(x))
+    got = bufs.o.cpu().numpy()
+    ref, heads, ref_u = _decode_refs(x, x.c_kv, x.k_pe, 2)
+    assert_tol(got, ref, TOL_BF16, "decode o")
+    assert_tol(got[[0, -1]][:, heads], ref_u, TOL_BF16, "decode o (un-absorbed heads)")
+
+
+@pytest.mark.parametrize("lengths", [[1], [1, 2, 3], [2049, 4096, 17, 6000], [5000] * 3])
+def test_decode_chain_ragged_lengths(lengths):
+    x = W.make_inputs("v3_decode_b32", n_head=32, lengths=lengths)
+    bufs = run_decode(Dev(x))
+    ref, heads, ref_u = _decode_refs(x, x.c_kv, x.k_pe)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_BF16, "decode o")
+
+
+def test_decode_equals_last_prefill_row_on_gpu():
+    x = W.make_inputs("lite_t256", T=300, n_kv=300, n_head=16)
+    d = Dev(x)
+    pre = run_prefill(d, 0)
+    xd = W.Inputs(W.make_inputs("v3_decode_b32", n_head=16, lengths=[300]).wl, x.c_kv, x.k_pe,
+                  x.q_nope[-1:], x.q_pe[-1:], x.wk_b, x.wv_b, np.array([300], np.int32), np.array([0], np.int64))
+    dd = Dev(xd)
+    dec = run_decode(dd)
+    a, b = pre.o.cpu().numpy()[-1], dec.o.cpu().numpy()[0]
+    assert_tol(b, a, (2e-3, 5e-4), "decode vs last prefill row")
+
+
+# ---------------------------------------------------------------------------
+# q8_0 cache
+# ---------------------------------------------------------------------------
+def test_quantize_q8_0_bit_exact():
+    rng = np.random.default_rng(9)
+    x = W.normal_bf16(rng, (1000, 576))
+    x[3] = 0.0                                       # all-zero row: codes 0, scale 0
+    x[5, :32] = np.float32(1e-30)                    # tiny block
+    x[7, 64:96] *= 1000.0                            # large block
+    x = W.to_bf16(x)[0]
+    codes, scales = O.quantize_q8_0(x)
+    kv = bf16_dev(x)
+    kv_q = torch.empty(1000, 576, dtype=torch.int8, device="cuda")
+    kv_d = torch.empty(18, 1024, dtype=torch.float16, device="cuda")
+    mla.mla_quantize_q8_0(kv, kv_q, kv_d)
+    np.testing.assert_array_equal(kv_q.cpu().numpy(), codes)
+    np.testing.assert_array_equal(kv_d.cpu().numpy()[:, :1000].view(np.uint16), scales.T.view(np.uint16))
+    _check_no_device_error()
+
+
+def _q8(x: W.Inputs):
+    codes, scales = O.quantize_q8_0(np.concatenate([x.c_kv, x.k_pe], axis=1))
+    deq = O.dequantize_q8_0(codes, scales)
+    return (codes, scales), deq[:, :512], deq[:, 512:]
+
+
+def test_prefill_chain_q8_small_every_row():
+    x = W.make_inputs("v3_q8_chunk8192_at90112", n_head=16, T=200, q_pos0=57, n_kv=300)
+    q8, c_kv, k_pe = _q8(x)
+    bufs = run_prefill(Dev(x, q8), x.wl.q_pos0, q8=True)
+    ref, _ = O.attention_unabsorbed(x.q_nope, x.q_pe, c_kv, k_pe, x.wk_b, x.wv_b, x.q_pos(), x.wl.scale)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_Q8, "q8 prefill o")
+
+
+def test_full_prefill_q8_chunk_sampled_rows():
+    x = W.make_inputs("v3_q8_chunk8192_at90112")
+    q8, c_kv, k_pe = _q8(x)
+    bufs = run_prefill(Dev(x, q8), x.wl.q_pos0, q8=True)
+    rows = sampled_rows(x.wl.T, x.wl.q_pos0)
+    ref, _ = O.attention_unabsorbed(x.q_nope[rows], x.q_pe[rows], c_kv, k_pe, x.wk_b, x.wv_b,
+                                    x.q_pos()[rows], x.wl.scale)
+    assert_tol(bufs.o.cpu().numpy()[rows], ref, TOL_Q8, "q8 chunk o")
+
+
+def test_decode_chain_q8_b8_every_sequence():
+    x = W.make_inputs("v3_q8_decode_b8")
+    q8, c_kv, k_pe = _q8(x)
+    bufs = run_decode(Dev(x, q8), q8=True)
+    got = bufs.o.cpu().numpy()
+    ref, heads, ref_u = _decode_refs(x, c_kv, k_pe, 2)
+    assert_tol(got, ref, TOL_Q8, "q8 decode o")
+    assert_tol(got[[0, -1]][:, heads], ref_u, TOL_Q8, "q8 decode o (un-absorbed heads)")
+
+
+def test_decode_q8_small_ragged():
+    x = W.make_inputs("v3_q8_decode_b8", n_head=16, lengths=[1, 33, 2050])
+    q8, c_kv, k_pe = _q8(x)
+    bufs = run_decode(Dev(x, q8), q8=True)
+    ref, _, _ = _decode_refs(x, c_kv, k_pe)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_Q8, "q8 decode o")
+
+
+# ---------------------------------------------------------------------------
+# Invariants on the GPU
+# ---------------------------------------------------------------------------
+def test_prefill_is_deterministic_and_causal():
+    x = W.make_inputs("lite_t256", T=200, q_pos0=100, n_kv=400)
+    d = Dev(x)
+    a = run_prefill(d, 100).o_lat.clone()
+    b = run_prefill(d, 100).o_lat.clone()
+    assert torch.equal(a, b)
+    # rows past the last query's position are never read: garbage there changes nothing
+    d.kv[300:] = float("nan")
+    c = run_prefill(d, 100).o_lat.clone()
+    assert torch.equal(a, c)
+
+
+def test_wait_timeout_is_reported_and_cleared():
+    assert mla.mla_get_device_error() == 0
+    mla.mla_selftest_wait_timeout(1000)
+    assert mla.mla_get_device_error() == -6          # MLA_ERR_TIMEOUT
+    assert mla.mla_get_device_error() == 0           # read clears it
+    x = W.make_inputs("lite_t256", T=16, n_kv=16)
+    run_prefill(Dev(x), 0)                           # the context is still usable
+
+
+def test_invalid_arguments_return_status():
+    x = W.make_inputs("lite_t256", T=8, n_kv=8)
+    d = Dev(x)
+    o_lat = torch.empty(8, 16, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_attn_prefill(bf16_dev(np.zeros((8, 16, 512), np.float32)), d.q_pe, d.kv, 1, o_lat)
+    assert e.value.status == -1                      # q_pos0 + T > n_kv
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_attn_decode(o_lat[:1], d.q_pe[:1], d.kv, torch.zeros(1, dtype=torch.int64, device="cuda"),
+                            torch.ones(1, dtype=torch.int32, device="cuda"), 8, ws, o_lat[:1])
+    assert e.value.status == -4                      # workspace too small
+    _check_no_device_error()
