@@ -23,6 +23,12 @@
  *   allocated, owned and freed by the caller.  No entry point allocates
  *   device or host memory, and none keeps a pointer after it returns.
  * - bf16 buffers are raw bfloat16 bit patterns (uint16_t); fp16 likewise.
+ * - Inputs taken from the model (queries, cache, weights) are bf16.  The two
+ *   intermediates of the path, q_lat and o_lat, are fp16: the attention
+ *   contractions run on fp16 tensor-core operands (bf16 cache rows are
+ *   converted on load, exactly for values inside the fp16 range), because
+ *   rounding q_lat, P and o_lat to bf16 alone would cost about 2.8e-3 mean
+ *   relative error of o, against about 0.6e-3 with fp16.
  * - Every device pointer must be 16-byte aligned (MLA_ERR_MISALIGNED).
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Work is enqueued asynchronously on it; host arguments are
@@ -82,7 +88,7 @@ typedef enum mla_status {
  *   q_lat[t][h][c] = sum_d q_nope[t][h][d] * wk_b[h][d][c]
  * q_nope  device bf16 [T][H][128]
  * wk_b    device bf16 [H][128][512]   (K up-projection, per head)
- * q_lat   device bf16 [T][H][512]     output, fp32 accumulation, rounded once
+ * q_lat   device fp16 [T][H][512]     output, fp32 accumulation, rounded once
  * T >= 1.                                                                     */
 int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b,
                  void* q_lat, int32_t T, void* stream);
@@ -91,10 +97,10 @@ int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b,
  *   s[t][h][j] = scale * (q_pe[t][h] . k_pe[j] + q_lat[t][h] . c_kv[j])
  *   visible iff j <= q_pos0 + t   (query t sits at position q_pos0 + t)
  *   o_lat[t][h] = sum_j softmax_j(s[t][h]) * c_kv[j]
- * q_lat   device bf16 [T][H][512]
+ * q_lat   device fp16 [T][H][512]
  * q_pe    device bf16 [T][H][64]
  * kv      device bf16 [n_kv][576]    latent cache (layout above)
- * o_lat   device bf16 [T][H][512]    output
+ * o_lat   device fp16 [T][H][512]    output
  * lse     device fp32 [T][H] or NULL; natural-log sum_j exp(s[t][h][j])
  * Requires T >= 1, q_pos0 >= 0 and q_pos0 + T <= n_kv.  Rows past
  * q_pos0 + T - 1 are never read.                                              */
@@ -121,12 +127,12 @@ size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_le
  * log-sum-exp combine of the partial results:
  *   sequence b's cache rows are kv[seq_start[b] .. seq_start[b] + seq_len[b]),
  *   its query sits at position seq_len[b] - 1 and sees all of them.
- * q_lat      device bf16 [B][H][512];  q_pe device bf16 [B][H][64]
+ * q_lat      device fp16 [B][H][512];  q_pe device bf16 [B][H][64]
  * kv         device bf16 [n_rows][576] (rows of all sequences)
  * seq_start  device int64 [B]  first row of each sequence
  * seq_len    device int32 [B]  1 <= seq_len[b] <= max_len, rows inside kv
  * workspace  device, ws_bytes >= mla_decode_workspace_size(dims, B, max_len)
- * o_lat      device bf16 [B][H][512]  output
+ * o_lat      device fp16 [B][H][512]  output
  * n_rows is the row count of kv (used for argument checks and the q8_0
  * scale layout).  seq_start/seq_len are read on the device only.              */
 int mla_attn_decode(const mla_dims* dims, const void* q_lat, const void* q_pe,
@@ -144,7 +150,7 @@ int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_
 
 /* Step 5, late decompression (method page sec. 4, the wv_b line):
  *   o[t][h][e] = sum_c o_lat[t][h][c] * wv_b[h][c][e]
- * o_lat device bf16 [T][H][512]; wv_b device bf16 [H][512][128];
+ * o_lat device fp16 [T][H][512]; wv_b device bf16 [H][512][128];
  * o     device fp32 [T][H][128] output.  T >= 1.                              */
 int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b,
                         float* o, int32_t T, void* stream);

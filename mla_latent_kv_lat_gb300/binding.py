@@ -116,14 +116,14 @@ def mla_absorb_q(q_nope: torch.Tensor, wk_b: torch.Tensor, q_lat: torch.Tensor, 
     d = make_dims(H, scale)
     args = (_need(q_nope, "q_nope", torch.bfloat16, (T, H, QK_NOPE)),
             _need(wk_b, "wk_b", torch.bfloat16, (H, QK_NOPE, KV_LORA_RANK)),
-            _need(q_lat, "q_lat", torch.bfloat16, (T, H, KV_LORA_RANK)))
+            _need(q_lat, "q_lat", torch.float16, (T, H, KV_LORA_RANK)))
     _check("mla_absorb_q", load_library().mla_absorb_q(ctypes.byref(d), *args, T, _stream(stream)))
 
 
 def mla_late_decompress(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor, scale=None, stream=None):
     T, H = o_lat.shape[0], o_lat.shape[1]
     d = make_dims(H, scale)
-    args = (_need(o_lat, "o_lat", torch.bfloat16, (T, H, KV_LORA_RANK)),
+    args = (_need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)),
             _need(wv_b, "wv_b", torch.bfloat16, (H, KV_LORA_RANK, V_HEAD)),
             _need(o, "o", torch.float32, (T, H, V_HEAD)))
     _check("mla_late_decompress", load_library().mla_late_decompress(ctypes.byref(d), *args, T, _stream(stream)))
@@ -135,9 +135,9 @@ def mla_attn_prefill(q_lat, q_pe, kv, q_pos0: int, o_lat, lse=None, scale=None, 
     d = make_dims(H, scale)
     lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
     st = load_library().mla_attn_prefill(
-        ctypes.byref(d), _need(q_lat, "q_lat", torch.bfloat16, (T, H, KV_LORA_RANK)),
+        ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (T, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv, "kv", torch.bfloat16, (n_kv, ROW)),
-        n_kv, T, q_pos0, _need(o_lat, "o_lat", torch.bfloat16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
+        n_kv, T, q_pos0, _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
     _check("mla_attn_prefill", st)
 
 
@@ -147,10 +147,10 @@ def mla_attn_prefill_q8_0(q_lat, q_pe, kv_q, kv_d, q_pos0: int, o_lat, lse=None,
     d = make_dims(H, scale)
     lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
     st = load_library().mla_attn_prefill_q8_0(
-        ctypes.byref(d), _need(q_lat, "q_lat", torch.bfloat16, (T, H, KV_LORA_RANK)),
+        ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (T, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv_q, "kv_q", torch.int8, (n_kv, ROW)),
         _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_kv)), n_kv, T, q_pos0,
-        _need(o_lat, "o_lat", torch.bfloat16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
+        _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
     _check("mla_attn_prefill_q8_0", st)
 
 
@@ -163,11 +163,11 @@ def mla_attn_decode(q_lat, q_pe, kv, seq_start, seq_len, max_len: int, workspace
     B, H = q_lat.shape[0], q_lat.shape[1]
     d = make_dims(H, scale)
     st = load_library().mla_attn_decode(
-        ctypes.byref(d), _need(q_lat, "q_lat", torch.bfloat16, (B, H, KV_LORA_RANK)),
+        ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (B, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (B, H, QK_ROPE)), _need(kv, "kv", torch.bfloat16),
         kv.shape[0], _need(seq_start, "seq_start", torch.int64, (B,)), _need(seq_len, "seq_len", torch.int32, (B,)),
         B, max_len, _need(workspace, "workspace", torch.uint8), workspace.numel(),
-        _need(o_lat, "o_lat", torch.bfloat16, (B, H, KV_LORA_RANK)), _stream(stream))
+        _need(o_lat, "o_lat", torch.float16, (B, H, KV_LORA_RANK)), _stream(stream))
     _check("mla_attn_decode", st)
 
 
@@ -177,12 +177,12 @@ def mla_attn_decode_q8_0(q_lat, q_pe, kv_q, kv_d, seq_start, seq_len, max_len: i
     n_rows = kv_q.shape[0]
     d = make_dims(H, scale)
     st = load_library().mla_attn_decode_q8_0(
-        ctypes.byref(d), _need(q_lat, "q_lat", torch.bfloat16, (B, H, KV_LORA_RANK)),
+        ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (B, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (B, H, QK_ROPE)), _need(kv_q, "kv_q", torch.int8, (n_rows, ROW)),
         _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_rows)), n_rows,
         _need(seq_start, "seq_start", torch.int64, (B,)), _need(seq_len, "seq_len", torch.int32, (B,)),
         B, max_len, _need(workspace, "workspace", torch.uint8), workspace.numel(),
-        _need(o_lat, "o_lat", torch.bfloat16, (B, H, KV_LORA_RANK)), _stream(stream))
+        _need(o_lat, "o_lat", torch.float16, (B, H, KV_LORA_RANK)), _stream(stream))
     _check("mla_attn_decode_q8_0", st)
 
 

@@ -162,7 +162,7 @@ int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32
   if (s != MLA_OK) return s;
   if (T < 1) return MLA_ERR_INVALID_ARG;
   if ((T + 63) / 64 > 65535) return MLA_ERR_UNSUPPORTED;
-  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0};
+  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, f32 ? 1 : 0};
   return to_status(launch_head_gemm_simt(g, static_cast<cudaStream_t>(stream)));
 }
 

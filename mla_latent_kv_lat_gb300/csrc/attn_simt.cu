@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
   for (int idx = tid; idx < kG * kRow; idx += kThreads) {
     const int r = idx / kRow, c = idx % kRow;
     const int64_t qi = q_row * H + h0 + r;
-    const uint16_t v = c < kLatent ? ql[qi * kLatent + c] : qp[qi * kRope + (c - kLatent)];
-    sm.q[idx] = bf16_to_f32(v) * qs;
+    const float v = c < kLatent ? f16_to_f32(ql[qi * kLatent + c]) : bf16_to_f32(qp[qi * kRope + (c - kLatent)]);
+    sm.q[idx] = v * qs;
   }
 
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
     const float inv = 1.f / sm.l[pr];
     uint16_t* o = static_cast<uint16_t*>(a.o_lat) + orow * kLatent;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[pc + 16 * i] = f32_to_bf16(acc[i] * inv);
+    for (int i = 0; i < 32; ++i) o[pc + 16 * i] = f32_to_f16(acc[i] * inv);
     if (a.lse != nullptr && pc == 0) a.lse[orow] = (sm.m[pr] + log2f(sm.l[pr])) * kLn2;
   } else {
     const int64_t slot = part * H + h0 + pr;
@@ -208,7 +208,7 @@ cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStr
 
 // ---------------------------------------------------------------------------
 // Split-KV combine: merge the per-split (m, l, o) of each (sequence, head) by
-// log-sum-exp and write o_lat in bf16.
+// log-sum-exp and write o_lat in fp16.
 // ---------------------------------------------------------------------------
 namespace {
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
   const float inv = 1.f / L;
   uint16_t* out = static_cast<uint16_t*>(c.o_lat) + (static_cast<int64_t>(b) * c.n_head + h) * kLatent + col;
   uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  pk.x = pack_f16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_f16x2(acc.z * inv, acc.w * inv);
   *reinterpret_cast<uint2*>(out) = pk;
 }
 }  // namespace

@@ -40,6 +40,19 @@ MLA_DEVINL float2 bf16x2_to_f32(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+MLA_DEVINL float f16_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+MLA_DEVINL uint16_t f32_to_f16(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+MLA_DEVINL uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+MLA_DEVINL float2 f16x2_to_f32(uint32_t w) {
+  return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+
 MLA_DEVINL uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }

@@ -7,7 +7,7 @@ namespace mla {
 
 // Arguments of one latent-attention launch (prefill or decode partials).
 struct AttnArgs {
-  const void* q_lat;        // bf16 [rows][H][512]
+  const void* q_lat;        // fp16 [rows][H][512]
   const void* q_pe;         // bf16 [rows][H][64]
   const void* kv;           // bf16 [n_rows][576]            (bf16 cache)
   const int8_t* kv_q;       // int8 [n_rows][576]            (q8_0 cache)
@@ -17,7 +17,7 @@ struct AttnArgs {
   float scale;
   // prefill
   int q_pos0;
-  void* o_lat;              // bf16 [T][H][512]
+  void* o_lat;              // fp16 [T][H][512]
   float* lse;               // fp32 [T][H] or null
   // decode
   int decode;
@@ -39,14 +39,15 @@ struct CombineArgs {
   int B, n_head, n_split, chunk;
 };
 
-// C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: K=128, N=512, bf16 out;
-// late decompression: K=512, N=128, fp32 out).
+// C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: bf16 A, K=128, N=512,
+// fp16 out; late decompression: fp16 A, K=512, N=128, fp32 out).  W is bf16.
 struct HeadGemmArgs {
-  const void* a;            // bf16 [T][H][K]
+  const void* a;            // bf16 or fp16 [T][H][K]
   const void* w;            // bf16 [H][K][N]
-  void* c;                  // bf16 or fp32 [T][H][N]
+  void* c;                  // fp16 or fp32 [T][H][N]
   int T, H, K, N;
   int out_f32;
+  int a_f16;
 };
 
 cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStream_t stream);

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) head_gemm_simt_kernel(HeadGemmArgs g) {
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 f = bf16x2_to_f32(w[e]);
+        const float2 f = g.a_f16 ? f16x2_to_f32(w[e]) : bf16x2_to_f32(w[e]);
         As[kc + 2 * e][t] = f.x;
         As[kc + 2 * e + 1][t] = f.y;
       }
@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(256) head_gemm_simt_kernel(HeadGemmArgs g) {
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     } else {
       uint2 pk;
-      pk.x = pack_bf16x2(acc[i][0], acc[i][1]);
-      pk.y = pack_bf16x2(acc[i][2], acc[i][3]);
+      pk.x = pack_f16x2(acc[i][0], acc[i][1]);
+      pk.y = pack_f16x2(acc[i][2], acc[i][3]);
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(g.c) + base) = pk;
     }
   }

@@ -18,16 +18,16 @@ from . import binding as B
 
 @dataclass
 class PrefillBuffers:
-    q_lat: torch.Tensor      # bf16 [T, H, 512]
-    o_lat: torch.Tensor      # bf16 [T, H, 512]
+    q_lat: torch.Tensor      # fp16 [T, H, 512]
+    o_lat: torch.Tensor      # fp16 [T, H, 512]
     o: torch.Tensor          # fp32 [T, H, 128]
     lse: Optional[torch.Tensor] = None
 
 
 def prefill_buffers(T: int, H: int, device="cuda", with_lse=False) -> PrefillBuffers:
     return PrefillBuffers(
-        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
-        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
+        torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
         torch.empty(T, H, B.V_HEAD, dtype=torch.float32, device=device),
         torch.empty(T, H, dtype=torch.float32, device=device) if with_lse else None)
 
@@ -61,8 +61,8 @@ class DecodeBuffers:
 def decode_buffers(Bn: int, H: int, max_len: int, device="cuda") -> DecodeBuffers:
     ws = B.mla_decode_workspace_size(H, Bn, max_len)
     return DecodeBuffers(
-        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
-        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.bfloat16, device=device),
+        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
+        torch.empty(Bn, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
         torch.empty(Bn, H, B.V_HEAD, dtype=torch.float32, device=device),
         torch.empty(ws, dtype=torch.uint8, device=device))
 

@@ -52,6 +52,12 @@ def to_bf16(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return vals, bits
 
 
+def to_f16(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Round fp32 ``x`` to IEEE half (nearest, ties to even): ``(values, bits)``."""
+    h = np.ascontiguousarray(x, dtype=np.float32).astype(np.float16)
+    return h.astype(np.float32), h.view(np.uint16)
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
@@ -135,6 +141,14 @@ def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray
     if std != 1.0:
         x *= np.float32(std)
     return to_bf16(x)[0]
+
+
+def normal_f16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std) fp32 draws rounded to fp16 (values as float32)."""
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return to_f16(x)[0]
 
 
 def decode_lengths(wl: Workload, seed: int = 0) -> np.ndarray:

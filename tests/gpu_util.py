@@ -17,6 +17,11 @@ def bf16_dev(vals: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(bits).view(torch.bfloat16).cuda()
 
 
+def f16_dev(vals: np.ndarray) -> torch.Tensor:
+    bits = W.to_f16(vals)[1]
+    return torch.from_numpy(bits).view(torch.float16).cuda()
+
+
 def dev_f32(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 

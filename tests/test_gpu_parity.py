@@ -12,7 +12,7 @@ import torch
 import mla_latent_kv_lat_gb300 as mla
 from mla_latent_kv_lat_gb300 import workloads as W
 from oracle import mla_oracle as O
-from tests.gpu_util import TOL_BF16, TOL_Q8, Dev, assert_tol, bf16_dev, dev_f32
+from tests.gpu_util import TOL_BF16, TOL_Q8, Dev, assert_tol, bf16_dev, dev_f32, f16_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -70,22 +70,22 @@ def sampled_rows(T, q_pos0, k=512, tile=128):
 def test_absorb_q_matches_oracle(H, T):
     x = W.make_inputs("v3_chunk8192_at32768", n_head=H, T=T, q_pos0=0, n_kv=T)
     q_nope, wk_b = bf16_dev(x.q_nope), bf16_dev(x.wk_b)
-    q_lat = torch.empty(T, H, 512, dtype=torch.bfloat16, device="cuda")
+    q_lat = torch.empty(T, H, 512, dtype=torch.float16, device="cuda")
     mla.mla_absorb_q(q_nope, wk_b, q_lat)
     got = dev_f32(q_lat)
     ref = O.absorb_q(x.q_nope, x.wk_b)
-    # one bf16 rounding of an fp32 sum of 128 products
-    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * np.sqrt(np.mean(ref ** 2)))
+    # one fp16 rounding (half an ulp = 2^-11 relative) of an fp32 sum of 128 exact products
+    assert np.all(np.abs(got - ref) <= 2.0 ** -10 * np.abs(ref) + 1e-5 * np.sqrt(np.mean(ref ** 2)))
     _check_no_device_error()
 
 
 @pytest.mark.parametrize("H,T", [(16, 1), (16, 77), (128, 200), (32, 64)])
 def test_late_decompress_matches_oracle(H, T):
     rng = np.random.default_rng(5)
-    o_lat = W.normal_bf16(rng, (T, H, 512), 0.3)
+    o_lat = W.normal_f16(rng, (T, H, 512), 0.3)
     wv_b = W.normal_bf16(rng, (H, 512, 128), 1 / np.sqrt(512))
     o = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
-    mla.mla_late_decompress(bf16_dev(o_lat), bf16_dev(wv_b), o)
+    mla.mla_late_decompress(f16_dev(o_lat), bf16_dev(wv_b), o)
     got = o.cpu().numpy().astype(np.float64)
     ref = O.late_decompress(o_lat, wv_b)
     # fp32 accumulation of 512 bf16 x bf16 products (products exact in fp32)
@@ -98,11 +98,11 @@ def test_late_decompress_matches_oracle(H, T):
 def test_prefill_latent_attention_matches_oracle(H, T, q_pos0, n_kv):
     x = W.make_inputs("lite_t256", n_head=H, T=T, q_pos0=q_pos0, n_kv=n_kv)
     rng = np.random.default_rng(3)
-    q_lat = W.normal_bf16(rng, (T, H, 512))
+    q_lat = W.normal_f16(rng, (T, H, 512))
     d = Dev(x)
-    o_lat = torch.empty(T, H, 512, dtype=torch.bfloat16, device="cuda")
+    o_lat = torch.empty(T, H, 512, dtype=torch.float16, device="cuda")
     lse = torch.empty(T, H, dtype=torch.float32, device="cuda")
-    mla.mla_attn_prefill(bf16_dev(q_lat), d.q_pe, d.kv, q_pos0, o_lat, lse)
+    mla.mla_attn_prefill(f16_dev(q_lat), d.q_pe, d.kv, q_pos0, o_lat, lse)
     ref, ref_lse = O.attention_latent(q_lat, x.q_pe, x.c_kv, x.k_pe, x.q_pos(), x.wl.scale)
     assert_tol(dev_f32(o_lat), ref, TOL_BF16, "o_lat")
     assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 2e-3
@@ -266,9 +266,9 @@ def test_wait_timeout_is_reported_and_cleared():
 def test_invalid_arguments_return_status():
     x = W.make_inputs("lite_t256", T=8, n_kv=8)
     d = Dev(x)
-    o_lat = torch.empty(8, 16, 512, dtype=torch.bfloat16, device="cuda")
+    o_lat = torch.empty(8, 16, 512, dtype=torch.float16, device="cuda")
     with pytest.raises(mla.MLAError) as e:
-        mla.mla_attn_prefill(bf16_dev(np.zeros((8, 16, 512), np.float32)), d.q_pe, d.kv, 1, o_lat)
+        mla.mla_attn_prefill(f16_dev(np.zeros((8, 16, 512), np.float32)), d.q_pe, d.kv, 1, o_lat)
     assert e.value.status == -1                      # q_pos0 + T > n_kv
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(mla.MLAError) as e:
