@@ -161,9 +161,10 @@ int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32
   s = check_ptrs({a, w, c});
   if (s != MLA_OK) return s;
   if (T < 1) return MLA_ERR_INVALID_ARG;
-  if ((T + 63) / 64 > 65535) return MLA_ERR_UNSUPPORTED;
+  int* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
   HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, f32 ? 1 : 0};
-  return to_status(launch_head_gemm_simt(g, static_cast<cudaStream_t>(stream)));
+  return to_status(launch_head_gemm_tc(g, err, kDefaultWaitPolls, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = tt * 128 + q * 32 + lane;
       for (int j = 0; ok && j < C::NS; ++j) {
         const int job = i * C::NS + j, slot = job % C::SLOTS;
-        ok = mbar_wait_bounded(&acc_full[slot], (job / C::SLOTS) & 1, g.polls, g.err);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[slot], (job / C::SLOTS) & 1, g.polls, g.err));
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1

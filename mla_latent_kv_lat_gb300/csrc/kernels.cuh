@@ -53,7 +53,8 @@ struct HeadGemmArgs {
 cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStream_t stream);
 size_t attn_simt_smem_bytes();
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
-cudaError_t launch_head_gemm_simt(const HeadGemmArgs& g, cudaStream_t stream);
+cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cudaStream_t stream);
+int device_sm_count();
 cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d,
                                  cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t stream);
