@@ -50,6 +50,8 @@ int check_ptrs(std::initializer_list<const void*> ps) {
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
+constexpr float kLog2eF = 1.4426950408889634f;
+
 // Split-KV plan of the decode kernels: keys per split and splits per sequence.
 struct DecodePlan {
   int chunk;
@@ -82,7 +84,7 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   int* err = nullptr;
   cudaError_t e = error_word(&err);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  AttnArgs a = {};
+  AttnTcArgs a = {};
   a.q_lat = q_lat;
   a.q_pe = q_pe;
   a.kv = kv;
@@ -90,14 +92,16 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   a.kv_d = kv_d;
   a.ld_d = n_kv;
   a.n_head = dims->n_head;
-  a.scale = dims->scale;
+  a.scale_log2 = dims->scale * kLog2eF;
   a.q_pos0 = q_pos0;
+  a.n_qrows = static_cast<int64_t>(T) * dims->n_head;
   a.o_lat = o_lat;
   a.lse = lse;
-  a.decode = 0;
   a.err = err;
-  a.wait_polls = kDefaultWaitPolls;
-  return to_status(launch_attn_simt(a, q8, T, static_cast<cudaStream_t>(stream)));
+  a.polls = kDefaultWaitPolls;
+  const int64_t items = (a.n_qrows + attn_tc_rows_per_item() - 1) / attn_tc_rows_per_item();
+  if (items > (1 << 30)) return MLA_ERR_UNSUPPORTED;
+  return to_status(launch_attn_tc(a, q8, false, static_cast<int>(items), static_cast<cudaStream_t>(stream)));
 }
 
 int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, const int8_t* kv_q,
@@ -112,7 +116,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   if ((reinterpret_cast<uintptr_t>(seq_start) & 7u) || (reinterpret_cast<uintptr_t>(seq_len) & 3u))
     return MLA_ERR_MISALIGNED;
   if (B < 1 || max_len < 1 || n_rows < 1) return MLA_ERR_INVALID_ARG;
-  if (B > 65535) return MLA_ERR_UNSUPPORTED;
+  if (B > 65535 || static_cast<int64_t>(B) * decode_plan(max_len).n_split > (1 << 30)) return MLA_ERR_UNSUPPORTED;
   const size_t need = decode_ws_bytes(dims->n_head, B, max_len);
   if (workspace == nullptr || ws_bytes < need) return MLA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MLA_ERR_MISALIGNED;
@@ -121,7 +125,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   const DecodePlan plan = decode_plan(max_len);
   const size_t slots = static_cast<size_t>(B) * plan.n_split * dims->n_head;
-  AttnArgs a = {};
+  AttnTcArgs a = {};
   a.q_lat = q_lat;
   a.q_pe = q_pe;
   a.kv = kv;
@@ -129,8 +133,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.kv_d = kv_d;
   a.ld_d = n_rows;
   a.n_head = dims->n_head;
-  a.scale = dims->scale;
-  a.decode = 1;
+  a.scale_log2 = dims->scale * kLog2eF;
   a.seq_start = seq_start;
   a.seq_len = seq_len;
   a.n_split = plan.n_split;
@@ -138,9 +141,9 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.ws_o = static_cast<float*>(workspace);
   a.ws_ml = a.ws_o + slots * kLatent;
   a.err = err;
-  a.wait_polls = kDefaultWaitPolls;
+  a.polls = kDefaultWaitPolls;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = launch_attn_simt(a, q8, B * plan.n_split, st);
+  e = launch_attn_tc(a, q8, true, B * plan.n_split, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   CombineArgs c = {};
   c.ws_o = a.ws_o;

@@ -50,6 +50,35 @@ struct HeadGemmArgs {
   int a_f16;
 };
 
+// Arguments of the tensor-core latent attention (prefill or decode partials).
+struct AttnTcArgs {
+  const void* q_lat;        // fp16 [rows][H][512]
+  const void* q_pe;         // bf16 [rows][H][64]
+  const void* kv;           // bf16 [n_rows][576]
+  const int8_t* kv_q;       // int8 [n_rows][576]
+  const uint16_t* kv_d;     // fp16 [18][ld_d]
+  int64_t ld_d;
+  int n_head;
+  float scale_log2;         // softmax scale * log2(e)
+  // prefill
+  int q_pos0;
+  int64_t n_qrows;          // T * H
+  void* o_lat;              // fp16 [T][H][512]
+  float* lse;               // fp32 [T][H] or null
+  // decode
+  const int64_t* seq_start;
+  const int32_t* seq_len;
+  int n_split;
+  int chunk;
+  float* ws_o;              // fp32 [B * n_split][H][512]
+  float* ws_ml;             // fp32 [B * n_split][H][2]
+  int* err;
+  uint32_t polls;
+};
+
+cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream);
+int attn_tc_rows_per_item();
+
 cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStream_t stream);
 size_t attn_simt_smem_bytes();
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
