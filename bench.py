@@ -34,7 +34,7 @@ METRIC = "MLA attn TFLOP/s (prefill) & HBM GB/s (decode) on 1 GB300, % of roofli
 DEFAULT_WORKLOAD = "lite_t4096"
 DECODE_WORKLOAD = "v3_decode_b32"
 FLOP_PER_PAIR_HEAD = 2 * 576 + 2 * 512          # scores (576-d) + latent weighted sum (512-d)
-KERNEL_SOURCES = ["attn_simt.cu", "misc.cu", "api.cu", "kernels.cuh", "common.cuh"]
+KERNEL_SOURCES = ["attn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"]
 
 
 # ---------------------------------------------------------------------------
@@ -261,7 +261,7 @@ def run_ours(args, torch, dist, rank, world):
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} HBM copy"}
-    kname = "attn_simt_kernel"
+    kname = "attn_tc_kernel"
     roof["traffic"] = recorded_traffic(kname, wl.name)
     roof["kernel"] = kname
     roof["attn_ms"] = round(attn_avg, 4)
@@ -295,7 +295,7 @@ def secondary(args, torch, name, flush, pk, pk_kind):
     return {"workload": name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(ach / pk["hbm_gbs"], 4), "peak_kind": f"{pk_kind} HBM copy",
-                         "attn_ms": round(attn, 4), "kernel": "attn_simt_kernel+combine_kernel"},
+                         "attn_ms": round(attn, 4), "kernel": "attn_tc_kernel+combine_kernel"},
             "tflops": round(attn_flops(wl, x) / (attn * 1e-3) / 1e12, 2)}
 
 

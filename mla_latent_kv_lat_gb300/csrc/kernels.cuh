@@ -5,32 +5,6 @@
 
 namespace mla {
 
-// Arguments of one latent-attention launch (prefill or decode partials).
-struct AttnArgs {
-  const void* q_lat;        // fp16 [rows][H][512]
-  const void* q_pe;         // bf16 [rows][H][64]
-  const void* kv;           // bf16 [n_rows][576]            (bf16 cache)
-  const int8_t* kv_q;       // int8 [n_rows][576]            (q8_0 cache)
-  const uint16_t* kv_d;     // fp16 [18][ld_d]               (q8_0 cache)
-  int64_t ld_d;
-  int n_head;
-  float scale;
-  // prefill
-  int q_pos0;
-  void* o_lat;              // fp16 [T][H][512]
-  float* lse;               // fp32 [T][H] or null
-  // decode
-  int decode;
-  const int64_t* seq_start;
-  const int32_t* seq_len;
-  int n_split;              // splits per sequence
-  int chunk;                // keys per split
-  float* ws_o;              // fp32 [B][n_split][H][512] unnormalised partial sums
-  float* ws_ml;             // fp32 [B][n_split][H][2]   running max (log2 units), sum
-  int* err;                 // device error word
-  uint32_t wait_polls;
-};
-
 struct CombineArgs {
   const float* ws_o;
   const float* ws_ml;
@@ -79,8 +53,6 @@ struct AttnTcArgs {
 cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream);
 int attn_tc_rows_per_item();
 
-cudaError_t launch_attn_simt(const AttnArgs& a, bool q8, int n_blocks_x, cudaStream_t stream);
-size_t attn_simt_smem_bytes();
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
 cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cudaStream_t stream);
 int device_sm_count();

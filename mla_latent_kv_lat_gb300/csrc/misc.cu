@@ -1,4 +1,5 @@
-// The q8_0 cache quantiser and the bounded-wait self-test.
+// The split-KV combine of the decode partials, the q8_0 cache quantiser and
+// the bounded-wait self-test.
 #include "kernels.cuh"
 
 namespace mla {
@@ -55,5 +56,47 @@ cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t 
   wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(polls, err);
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------------------
+// Split-KV combine: merge the per-split (m, l, o) of each (sequence, head) by
+// log-sum-exp and write o_lat in fp16.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
+  const int b = blockIdx.x / c.n_head, h = blockIdx.x % c.n_head;
+  const int64_t len = c.seq_len[b];
+  const int ns = static_cast<int>(min(static_cast<int64_t>(c.n_split), (len + c.chunk - 1) / c.chunk));
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) {
+    const int64_t slot = (static_cast<int64_t>(b) * c.n_split + s) * c.n_head + h;
+    M = fmaxf(M, c.ws_ml[2 * slot]);
+  }
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int col = threadIdx.x * 4;
+  for (int s = 0; s < ns; ++s) {
+    const int64_t slot = (static_cast<int64_t>(b) * c.n_split + s) * c.n_head + h;
+    const float w = exp2f(c.ws_ml[2 * slot] - M);
+    L += w * c.ws_ml[2 * slot + 1];
+    const float4 o = *reinterpret_cast<const float4*>(c.ws_o + slot * kLatent + col);
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  const float inv = 1.f / L;
+  uint16_t* out = static_cast<uint16_t*>(c.o_lat) + (static_cast<int64_t>(b) * c.n_head + h) * kLatent + col;
+  uint2 pk;
+  pk.x = pack_f16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_f16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out) = pk;
+}
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream) {
+  combine_kernel<<<c.B * c.n_head, 128, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
 
 }  // namespace mla
