@@ -148,6 +148,33 @@ int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_
                          int32_t max_len, void* workspace, size_t ws_bytes,
                          void* o_lat, void* stream);
 
+/* Split-KV decode exactly as mla_attn_decode (bf16 cache), for callers that
+ * cannot allocate device memory: a plugin running inside a host engine that
+ * owns every device allocation and forbids cudaMalloc, or a caller with no
+ * allocator from which to take the decode workspace.  The pages have no
+ * counterpart to this entry point; it exists only for such callers.
+ * It takes no workspace: the split-KV partial results go to one fixed 32 MiB
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.  The entry point allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ * Limit: mla_decode_workspace_size(dims, B, max_len) must not exceed
+ *   33554432 bytes (32 MiB); larger requests return MLA_ERR_WORKSPACE with
+ *   nothing launched.  E.g. B = 8 sequences up to 16384 tokens at 128 heads
+ *   need 16.8 MB.
+ * Sharing: every call uses the same array.  Calls whose work overlaps on the
+ *   GPU (different streams without ordering, several host threads) race on it
+ *   and corrupt each other's results; order them on one stream or with
+ *   events.  Nothing in the array needs to start at zero: each call writes
+ *   every partial it later reads, so the previous call's contents do no harm.
+ * Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * Arguments, layouts and errors are otherwise those of mla_attn_decode.       */
+int mla_attn_decode_static(const mla_dims* dims, const void* q_lat, const void* q_pe,
+                           const void* kv, int64_t n_rows, const int64_t* seq_start,
+                           const int32_t* seq_len, int32_t B, int32_t max_len,
+                           void* o_lat, void* stream);
+
 /* Step 5, late decompression (method page sec. 4, the wv_b line):
  *   o[t][h][e] = sum_c o_lat[t][h][c] * wv_b[h][c][e]
  * o_lat device fp16 [T][H][512]; wv_b device bf16 [H][512][128];

@@ -52,6 +52,7 @@ _SIGS = {
     "mla_decode_workspace_size": ([_D, _I32, _I32], _SZ),
     "mla_attn_decode": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "mla_attn_decode_q8_0": ([_D, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
+    "mla_attn_decode_static": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P], ctypes.c_int),
     "mla_late_decompress": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
     "mla_quantize_q8_0": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "mla_get_device_error": ([_P], ctypes.c_int),
@@ -169,6 +170,18 @@ def mla_attn_decode(q_lat, q_pe, kv, seq_start, seq_len, max_len: int, workspace
         B, max_len, _need(workspace, "workspace", torch.uint8), workspace.numel(),
         _need(o_lat, "o_lat", torch.float16, (B, H, KV_LORA_RANK)), _stream(stream))
     _check("mla_attn_decode", st)
+
+
+def mla_attn_decode_static(q_lat, q_pe, kv, seq_start, seq_len, max_len: int, o_lat, scale=None, stream=None):
+    """Decode without a workspace argument (the library's fixed device scratch)."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    d = make_dims(H, scale)
+    st = load_library().mla_attn_decode_static(
+        ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (B, H, KV_LORA_RANK)),
+        _need(q_pe, "q_pe", torch.bfloat16, (B, H, QK_ROPE)), _need(kv, "kv", torch.bfloat16),
+        kv.shape[0], _need(seq_start, "seq_start", torch.int64, (B,)), _need(seq_len, "seq_len", torch.int32, (B,)),
+        B, max_len, _need(o_lat, "o_lat", torch.float16, (B, H, KV_LORA_RANK)), _stream(stream))
+    _check("mla_attn_decode_static", st)
 
 
 def mla_attn_decode_q8_0(q_lat, q_pe, kv_q, kv_d, seq_start, seq_len, max_len: int, workspace, o_lat,
