@@ -91,6 +91,7 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   a.kv_q = kv_q;
   a.kv_d = kv_d;
   a.ld_d = n_kv;
+  a.n_rows = static_cast<int64_t>(q_pos0) + T;     // rows past the last query are never read
   a.n_head = dims->n_head;
   a.scale_log2 = dims->scale * kLog2eF;
   a.q_pos0 = q_pos0;
@@ -116,6 +117,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   if ((reinterpret_cast<uintptr_t>(seq_start) & 7u) || (reinterpret_cast<uintptr_t>(seq_len) & 3u))
     return MLA_ERR_MISALIGNED;
   if (B < 1 || max_len < 1 || n_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (n_rows > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (B > 65535 || static_cast<int64_t>(B) * decode_plan(max_len).n_split > (1 << 30)) return MLA_ERR_UNSUPPORTED;
   const size_t need = decode_ws_bytes(dims->n_head, B, max_len);
   if (workspace == nullptr || ws_bytes < need) return MLA_ERR_WORKSPACE;
@@ -132,6 +134,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.kv_q = kv_q;
   a.kv_d = kv_d;
   a.ld_d = n_rows;
+  a.n_rows = n_rows;
   a.n_head = dims->n_head;
   a.scale_log2 = dims->scale * kLog2eF;
   a.seq_start = seq_start;

@@ -11,18 +11,28 @@
 //     memory, leaving no room for scores, so the pair splits the latent
 //     dimension: CTA r owns latent columns [256r, 256r+256) of the output and
 //     of the score contraction; CTA 0 also owns the 64 RoPE dimensions.
-//   * Each CTA computes its partial scores S_r = Q_r K_r^T on tcgen05 into
-//     TMEM, scales and rounds them to fp16 and sends them to its peer with
-//     st.async into distributed shared memory; both CTAs then hold the same
-//     fp16 pair and form identical scores, maxima and probabilities, so their
-//     output halves stay consistent without further exchange.
-//   * P (fp16) goes to shared memory and O_r += P V_r runs on tcgen05 with V_r
-//     read in place from the same cache tile (MN-major view).
-//   * Cache tiles are loaded by four producer warps, converted to fp16 on the
-//     way (bf16 cache: exact; q8_0 cache: fp16 scale x int8 code), and stored
-//     in the 128-byte-swizzled layout the tensor core reads.
-//   * Roles per CTA: warps 0-3 softmax / exchange / epilogue (thread = row),
-//     warps 4-7 producer, warp 8 MMA issue.  Every wait is bounded.
+//   * Each CTA computes its partial scores on tcgen05 into TMEM: the latent
+//     part as fp16 x fp16 with Q from TMEM, the RoPE part as bf16 x bf16 (the
+//     bf16 cache and q_pe enter it unrounded; with a q8_0 cache both are fp16)
+//     into the same fp32 accumulator.  The partial is rounded to fp16 and sent
+//     to the peer with st.async into distributed shared memory; both CTAs add
+//     the same two fp16 partials in fp32, so their scores, maxima and
+//     probabilities agree.
+//   * Score MMAs run three tiles ahead of the P.V MMAs: the softmax sends tile
+//     j+1's partial before it processes tile j, so the exchange latency and
+//     the score MMAs overlap the softmax.
+//   * P (fp16) goes to shared memory; O_r += P V_r runs on tcgen05 with V_r read
+//     in place from the latent cache tile (MN-major view).
+//   * Latent cache tiles are loaded by seven producer warps with
+//     software-pipelined 16-byte loads, converted to fp16 (bf16: exact; q8_0:
+//     fp16 scale x int8 code) and stored in the 128-byte-swizzled layout the
+//     tensor core reads.  The bf16 RoPE part arrives by TMA.
+//   * Roles per CTA: warps 0-7 softmax / exchange / epilogue (two threads per
+//     row, 32 keys of each 64-key tile each), warps 8-14 producer, warp 15 MMA
+//     issue.  Every wait is bounded; a failed wait is passed between the two
+//     warps that share rows so that both leave.
+#include <string.h>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -31,45 +41,55 @@ namespace {
 
 constexpr int kRows = 128;                   // query rows per cluster (MMA M)
 constexpr int kBK = 64;                      // keys per tile
-constexpr int kNChMax = 5;                   // 64-dim chunks per CTA (rank 0: 4 latent + rope)
-constexpr int kKvChunk = kBK * 128;          // 8 KB: 64 keys x 64 fp16
-constexpr int kKvStage = kNChMax * kKvChunk; // 40 KB
-constexpr int kStages = 3;
-constexpr int kQRopeBytes = kRows * 128;     // 16 KB: 128 rows x 64 fp16
+constexpr int kChunk = kBK * 128;            // 8 KB: 64 keys x 64 16-bit values
+constexpr int kLatStage = 4 * kChunk;        // 32 KB: this CTA's 256 latent dims
+constexpr int kLatStages = 4;
+constexpr int kRopeStages = 3;
+constexpr int kQRopeBytes = kRows * 128;     // 16 KB: 128 rows x 64 dims
 constexpr int kPBytes = kRows * 128;         // 16 KB: 128 rows x 64 keys fp16
-constexpr int kXBytes = kRows * kBK * 2;     // 16 KB: one exchange buffer
-constexpr int kOffKv = kQRopeBytes;
-constexpr int kOffP = kOffKv + kStages * kKvStage;
+constexpr int kXBytes = kRows * kBK * 2;     // 16 KB: one exchange buffer (fp16 partial scores)
+constexpr int kOffLat = kQRopeBytes;
+constexpr int kOffRope = kOffLat + kLatStages * kLatStage;
+constexpr int kOffP = kOffRope + kRopeStages * kChunk;
 constexpr int kOffX = kOffP + kPBytes;
-constexpr int kOffBar = kOffX + 2 * kXBytes;
+constexpr int kOffAux = kOffX + 2 * kXBytes;
+// row maxima [tile parity][half][row], row sums [half][row], failure flags [tile parity][warp]
+constexpr int kAuxBytes = (4 * kRows + 2 * kRows) * 4 + 16 * 4;
+constexpr int kOffBar = kOffAux + kAuxBytes;
 constexpr int kSmem = 1024 + kOffBar + 256;
-constexpr int kThreads = 288;
+constexpr int kSoftmaxWarps = 8, kProducerWarps = 7;
+constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;   // 512: four warps per SM sub-partition
+constexpr int kProducerThreads = kProducerWarps * 32;
 // TMEM columns: Q latent half (A operand, 256 fp16 = 128 cols), two fp32 score
 // buffers of 64 columns, the fp32 output half (256 cols).
 constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 256, exact in fp16
+constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 256 in fp16
 
 struct Bars {
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t lat_full[kLatStages];
+  uint64_t lat_empty[kLatStages];
+  uint64_t rope_full[kRopeStages];
+  uint64_t rope_empty[kRopeStages];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t x_full[2];
+  uint64_t x_empty[2];
   uint64_t p_full;
   uint64_t pv_done;
   uint64_t q_ready;
+  uint64_t pair[4];          // the two softmax warps that share 32 rows, once per tile
   uint32_t tmem;
-  int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(kSmem <= 232448, "shared memory");
 
 MLA_DEVINL bool wait_all(uint64_t* bar, uint32_t parity, const AttnTcArgs& a) {
   return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.polls, a.err));
 }
 
-// Store 8 halves (one 16-byte unit) to the swizzled K-major tile `base`
-// (rows of 128 B): row `row`, unit `u` (elements 8u..8u+7).
+// Store one 16-byte unit (8 halves) into a 128-byte-swizzled K-major tile.
 MLA_DEVINL void st_unit(uint8_t* base, int row, int u, uint4 v) {
   *reinterpret_cast<uint4*>(base + row * 128 + ((u ^ (row & 7)) << 4)) = v;
 }
@@ -90,18 +110,118 @@ MLA_DEVINL uint32_t i8x2_to_f16x2(uint32_t w, int sh, float d) {
   return pack_f16x2(a * d, b * d);
 }
 
+// ---------------------------------------------------------------------------
+// Producer: one 64-key tile of this CTA's cache part.
+//   bf16 cache: the 256 latent dims (32 units of 8 values per key); the RoPE
+//               part of rank 0 comes by TMA.
+//   q8_0 cache: the 256 latent dims (16 units of 16 codes per key) plus, on
+//               rank 0, the 64 RoPE dims (4 units), dequantised to fp16.
+// ---------------------------------------------------------------------------
+template <bool kQ8, bool kRope>
+struct Producer {
+  static constexpr int LAT_UPK = kQ8 ? 16 : 32;
+  static constexpr int UPK = LAT_UPK + ((kQ8 && kRope) ? 4 : 0);
+  static constexpr int NUNITS = kBK * UPK;
+  static constexpr int NU = (NUNITS + kProducerThreads - 1) / kProducerThreads;
+  uint4 v[NU];
+  float d[kQ8 ? NU : 1];
+
+  MLA_DEVINL void load(const AttnTcArgs& a, int rank, int pt, int64_t key_base, int k0, int kend) {
+#pragma unroll
+    for (int t = 0; t < NU; ++t) {
+      const int idx = pt + t * kProducerThreads;
+      const int key = idx / UPK, cu = idx % UPK;
+      v[t] = make_uint4(0, 0, 0, 0);
+      if constexpr (kQ8) d[t] = 0.f;
+      if (idx < NUNITS && k0 + key < kend) {
+        const int64_t row = key_base + k0 + key;
+        if constexpr (!kQ8) {
+          v[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.kv) + row * kRow + 256 * rank +
+                                                      cu * 8));
+        } else {
+          const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + (cu - 16) * 16;
+          v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
+          d[t] = __half2float(__ushort_as_half(__ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row)));
+        }
+      }
+    }
+  }
+
+  MLA_DEVINL void store(uint8_t* lat, uint8_t* rope, int pt) const {
+#pragma unroll
+    for (int t = 0; t < NU; ++t) {
+      const int idx = pt + t * kProducerThreads;
+      const int key = idx / UPK, cu = idx % UPK;
+      if (idx >= NUNITS) break;
+      if constexpr (!kQ8) {
+        st_unit(lat + (cu >> 3) * kChunk, key, cu & 7, bf16x8_to_f16x8(v[t]));
+      } else {
+        uint8_t* base = cu < 16 ? lat + (cu >> 2) * kChunk : rope;
+        const int u = (cu & 3) * 2;
+        uint4 lo, hi;
+        lo.x = i8x2_to_f16x2(v[t].x, 0, d[t]);  lo.y = i8x2_to_f16x2(v[t].x, 16, d[t]);
+        lo.z = i8x2_to_f16x2(v[t].y, 0, d[t]);  lo.w = i8x2_to_f16x2(v[t].y, 16, d[t]);
+        hi.x = i8x2_to_f16x2(v[t].z, 0, d[t]);  hi.y = i8x2_to_f16x2(v[t].z, 16, d[t]);
+        hi.z = i8x2_to_f16x2(v[t].w, 0, d[t]);  hi.w = i8x2_to_f16x2(v[t].w, 16, d[t]);
+        st_unit(base, key, u, lo);
+        st_unit(base, key, u + 1, hi);
+      }
+    }
+  }
+};
+
+template <bool kQ8, bool kRope>
+MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Bars& B, uint8_t* sLat,
+                             uint8_t* sRope, int rank, int pt, int64_t key_base, int kend, int n_tiles) {
+  using P = Producer<kQ8, kRope>;
+  P x, y;
+  // Tile j+1's loads are in flight while tile j is converted and stored.
+  auto step = [&](int j, P& cur, P& nxt) -> bool {
+    if (j + 1 < n_tiles) nxt.load(a, rank, pt, key_base, (j + 1) * kBK, kend);
+    const int ls = j % kLatStages, rs = j % kRopeStages;
+    if (j >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((j / kLatStages) - 1) & 1, a.polls, a.err))
+      return false;
+    if (kRope && j >= kRopeStages &&
+        !mbar_wait_bounded(&B.rope_empty[rs], ((j / kRopeStages) - 1) & 1, a.polls, a.err))
+      return false;
+    if constexpr (kRope && !kQ8) {            // bf16 RoPE keys by TMA, straight into the B-operand layout
+      if (pt == 0) {
+        mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
+        tc::tma_load_3d(sRope + rs * kChunk, tm_rope, &B.rope_full[rs], kLatent,
+                        static_cast<int>(key_base + j * kBK), 0);
+      }
+    }
+    cur.store(sLat + ls * kLatStage, sRope + rs * kChunk, pt);
+    tc::fence_proxy_async();
+    mbar_arrive(&B.lat_full[ls]);
+    return true;
+  };
+  if (n_tiles > 0) x.load(a, rank, pt, key_base, 0, kend);
+  for (int j = 0; j < n_tiles; j += 2) {
+    if (!step(j, x, y)) return;
+    if (j + 1 < n_tiles && !step(j + 1, y, x)) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
 template <bool kQ8, bool kDecode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_rope, AttnTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQr = sm;
-  uint8_t* sKV = sm + kOffKv;
+  uint8_t* sLat = sm + kOffLat;
+  uint8_t* sRope = sm + kOffRope;
   uint8_t* sP = sm + kOffP;
   uint8_t* sX = sm + kOffX;
+  float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][2][128] row maxima of both halves
+  float* aux_l = aux_m + 4 * kRows;                             // [2][128] row sums
+  int* aux_fail = reinterpret_cast<int*>(aux_l + 2 * kRows);    // [2][8] per-warp failure flags
   Bars& B = *reinterpret_cast<Bars*>(sm + kOffBar);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
-  const int nch = rank == 0 ? 5 : 4;          // 64-dim chunks of this CTA's score contraction
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.n_head;
 
@@ -133,22 +253,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
 
   // ---- setup -----------------------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&B.kv_full[i], 128);
-      mbar_init(&B.kv_empty[i], 1);
+    for (int i = 0; i < kLatStages; ++i) {
+      mbar_init(&B.lat_full[i], kProducerThreads);
+      mbar_init(&B.lat_empty[i], 1);
+    }
+    for (int i = 0; i < kRopeStages; ++i) {
+      mbar_init(&B.rope_full[i], 1);
+      mbar_init(&B.rope_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_free[i], 128);
+      mbar_init(&B.s_free[i], kSoftmaxWarps * 32);
       mbar_init(&B.x_full[i], 1);
+      mbar_init(&B.x_empty[i], kSoftmaxWarps);
     }
-    mbar_init(&B.p_full, 128);
+    mbar_init(&B.p_full, kSoftmaxWarps * 32);
     mbar_init(&B.pv_done, 1);
-    mbar_init(&B.q_ready, 128);
-    B.abort = 0;
+    mbar_init(&B.q_ready, kSoftmaxWarps * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&B.pair[i], 64);
     tc::fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&B.tmem, 512);
     tc::tmem_relinquish();
   }
@@ -157,39 +282,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
   tc::fence_after_sync();
   const uint32_t tmem = B.tmem;
 
-  if (warp < 4) {
+  if (warp < kSoftmaxWarps) {
     // ======================= softmax / exchange / epilogue =====================
-    const int i = threadIdx.x;        // query row of this thread == TMEM lane
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const int q4 = warp & 3;                    // TMEM lane quadrant
+    const int hh = warp >> 2;                   // key half of each tile: keys [32hh, 32hh+32)
+    const int partner = warp ^ 4;               // the warp holding the other 32 keys of these rows
+    const int i = q4 * 32 + lane;               // query row == TMEM lane
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
     const bool rvalid = i < nvalid;
     const int64_t qrow = qrow0 + i;
-    int lim;                          // last visible key index (item-relative)
+    int lim;                                    // last visible key index (item-relative)
     if constexpr (kDecode) {
       lim = kend - 1;
     } else {
       lim = rvalid ? a.q_pos0 + static_cast<int>(qrow / H) : kend - 1;
     }
-    // Q latent half -> TMEM (A operand: fp16 pairs, row = lane).
+    const float c2 = a.scale_log2;              // raw score -> log2 units
+    // Q latent half -> TMEM (fp16 A operand), this thread: dims [128hh, 128hh+128) of the half.
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
-                                                        256 * rank);
+                                                        256 * rank + 128 * hh);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = rvalid ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
           r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
         }
-        tc::tmem_st32(tmem + lanes + kTmQ + c * 32, r);
+        tc::tmem_st32(tmem + lanes + kTmQ + 64 * hh + 32 * c, r);
       }
       tc::tmem_st_wait();
-      if (rank == 0) {                // RoPE query part -> smem (bf16 -> fp16)
+      if (rank == 0) {                          // RoPE query part -> smem (bf16 as is; fp16 for q8_0)
         const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = rvalid ? __ldg(qp + u) : make_uint4(0, 0, 0, 0);
-          st_unit(sQr, i, u, bf16x8_to_f16x8(x));
+        for (int u = 0; u < 4; ++u) {
+          const uint4 x = rvalid ? __ldg(qp + 4 * hh + u) : make_uint4(0, 0, 0, 0);
+          st_unit(sQr, i, 4 * hh + u, kQ8 ? bf16x8_to_f16x8(x) : x);
         }
         tc::fence_proxy_async();
       }
@@ -198,111 +327,153 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
     }
 
     const uint32_t peer_x = tc::mapa(smem_u32(sX), peer);
-    const uint32_t peer_xbar = tc::mapa(smem_u32(&B.x_full[0]), peer);
-    const float sl = a.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t peer_xfull = tc::mapa(smem_u32(&B.x_full[0]), peer);
+    const uint32_t peer_xempty = tc::mapa(smem_u32(&B.x_empty[0]), peer);
+    float m_run = -INFINITY, l_h = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int b = j & 1;
-      ok = wait_all(&B.s_full[b], (j >> 1) & 1, a);
-      if (!ok) break;
+
+    // Read this thread's 32 partial scores of tile t, free the score buffer,
+    // keep them as fp16 pairs and send the same pairs to the peer.
+    auto fetch_send = [&](int t, uint32_t (&own)[16]) -> bool {
+      const int sb = t & 1;
+      if (!wait_all(&B.s_full[sb], (t >> 1) & 1, a)) return false;
       tc::fence_after_sync();
-      uint32_t own[32];
-      {
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld32(tmem + lanes + kTmS + b * 64, r0);
-        tc::tmem_ld32(tmem + lanes + kTmS + b * 64 + 32, r1);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        mbar_arrive(&B.s_free[b]);
+      uint32_t r[32];
+      tc::tmem_ld32(tmem + lanes + kTmS + sb * 64 + 32 * hh, r);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      mbar_arrive(&B.s_free[sb]);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          own[k] = pack_f16x2(__uint_as_float(r0[2 * k]) * sl, __uint_as_float(r0[2 * k + 1]) * sl);
-          own[16 + k] = pack_f16x2(__uint_as_float(r1[2 * k]) * sl, __uint_as_float(r1[2 * k + 1]) * sl);
-        }
-      }
-      // exchange the fp16 partial scores with the peer
+      for (int k = 0; k < 16; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+      if (t >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1,
+                                                                           a.polls, a.err)))
+        return false;
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        tc::st_async_v4(peer_x + b * kXBytes + (g * kRows + i) * 16,
-                        make_uint4(own[4 * g], own[4 * g + 1], own[4 * g + 2], own[4 * g + 3]),
-                        peer_xbar + b * 8);
-      if (i == 0) mbar_arrive_expect_tx(&B.x_full[b], kXBytes);
-      ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[b], (j >> 1) & 1, a.polls, a.err));
-      if (!ok) break;
-      float s[64];
-      float mt = -INFINITY;
+      for (int g = 0; g < 4; ++g)
+        tc::st_async_v4(peer_x + sb * kXBytes + ((4 * hh + g) * kRows + i) * 16,
+                        make_uint4(own[4 * g], own[4 * g + 1], own[4 * g + 2], own[4 * g + 3]), peer_xfull + sb * 8);
+      if (threadIdx.x == 0) mbar_arrive_expect_tx(&B.x_full[sb], kXBytes);
+      return true;
+    };
+
+    // Meet the partner warp (same rows, other key half) once per phase; a wait
+    // that gave up is passed on so that both warps leave together.
+    auto pair_sync = [&](int phase, bool ok_in) -> bool {
+      if (lane == 0) aux_fail[(phase & 1) * 8 + warp] = ok_in ? 0 : 1;
+      mbar_arrive(&B.pair[q4]);
+      const bool okp = wait_all(&B.pair[q4], phase & 1, a);
+      return okp && ok_in && aux_fail[(phase & 1) * 8 + partner] == 0;
+    };
+
+    // Softmax of tile j from the two fp16 partials.
+    auto process = [&](int j, const uint32_t (&own)[16]) -> bool {
+      const int xb = j & 1;
+      const bool okx =
+          __all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.polls, a.err));
+      float s[32];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint4 pv = *reinterpret_cast<const uint4*>(sX + b * kXBytes + (g * kRows + i) * 16);
+      for (int g = 0; g < 4; ++g) {
+        const uint4 pv = *reinterpret_cast<const uint4*>(sX + xb * kXBytes + ((4 * hh + g) * kRows + i) * 16);
         const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 x = f16x2_to_f32(own[4 * g + e]);
-          const float2 y = f16x2_to_f32(pw[e]);
-          const int k = 8 * g + 2 * e;
-          const int kk = j * kBK + k;
-          s[k] = kk <= lim ? x.x + y.x : -INFINITY;
-          s[k + 1] = kk + 1 <= lim ? x.y + y.y : -INFINITY;
-          mt = fmaxf(mt, fmaxf(s[k], s[k + 1]));
+          s[8 * g + 2 * e] = tc::add_f16lo_f32(pw[e], x.x);
+          s[8 * g + 2 * e + 1] = tc::add_f16hi_f32(pw[e], x.y);
         }
       }
-      const float m_new = fmaxf(m_run, mt);
-      const bool need = m_new > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = exp2f(m_run - m_new);
-        m_run = m_new;
+      __syncwarp();
+      if (okx && lane == 0) tc::mbar_arrive_remote(peer_xempty + xb * 8);   // this warp is done with buffer xb
+      const int k0 = j * kBK + 32 * hh;
+      if (k0 + 31 > lim) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (k0 + k > lim) s[k] = -INFINITY;
       }
-      const bool warp_need = __any_sync(0xffffffffu, need);
-      uint32_t pk[32];
+      float mt = s[0];
+#pragma unroll
+      for (int k = 1; k < 32; ++k) mt = fmaxf(mt, s[k]);
+      mt *= c2;
+      aux_m[((j & 1) * 2 + hh) * kRows + i] = mt;
+      if (!pair_sync(j, okx)) return false;
+      const float mrow = fmaxf(mt, aux_m[((j & 1) * 2 + (1 - hh)) * kRows + i]);
+      // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
+      float alpha = 1.f;
+      if (mrow > m_run + kRescaleThreshold) {
+        alpha = tc::exp2_approx(m_run - mrow);
+        m_run = mrow;
+        l_h *= alpha;
+      }
+      uint32_t pk[16];
       float lsum = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        pk[k] = pack_f16x2(exp2f(s[2 * k] - m_run), exp2f(s[2 * k + 1] - m_run));
-        const float2 f = f16x2_to_f32(pk[k]);
-        lsum += f.x + f.y;
+      for (int k = 0; k < 16; ++k) {
+        const float p0 = tc::exp2_approx(fmaf(s[2 * k], c2, -m_run));
+        const float p1 = tc::exp2_approx(fmaf(s[2 * k + 1], c2, -m_run));
+        lsum += p0 + p1;
+        pk[k] = pack_f16x2(p0, p1);
       }
-      l_run = l_run * alpha + lsum;
+      l_h += lsum;
+      // P.V of tile j-1 has finished: the P buffer is free and O is stable.
       if (j >= 1) {
-        ok = wait_all(&B.pv_done, (j - 1) & 1, a);
-        if (!ok) break;
+        if (!wait_all(&B.pv_done, (j - 1) & 1, a)) return false;
         tc::fence_after_sync();
-        if (warp_need) {              // rescale this warp's 32 output rows
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tc::tmem_ld32(tmem + lanes + kTmO + c * 32, o);
+            const uint32_t col = tmem + lanes + kTmO + 128 * hh + 32 * c;
+            tc::tmem_ld32(col, o);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st32(tmem + lanes + kTmO + c * 32, o);
+            tc::tmem_st32(col, o);
           }
           tc::tmem_st_wait();
         }
       }
 #pragma unroll
-      for (int g = 0; g < 8; ++g) st_unit(sP, i, g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+      for (int g = 0; g < 4; ++g)
+        st_unit(sP, i, 4 * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
       tc::fence_proxy_async();
       tc::fence_before_sync();
       mbar_arrive(&B.p_full);
+      return true;
+    };
+
+    uint32_t ownA[16], ownB[16];
+    ok = fetch_send(0, ownA);
+    for (int j = 0; ok && j < n_tiles; j += 2) {
+      if (j + 1 < n_tiles) ok = fetch_send(j + 1, ownB);
+      ok = ok && process(j, ownA);
+      if (!ok || j + 1 >= n_tiles) break;
+      if (j + 2 < n_tiles) ok = fetch_send(j + 2, ownA);
+      ok = ok && process(j + 1, ownB);
     }
     if (ok) ok = wait_all(&B.pv_done, (n_tiles - 1) & 1, a);
+    aux_l[hh * kRows + i] = l_h;
+    ok = pair_sync(n_tiles, ok);
     if (ok) {
       tc::fence_after_sync();
-      const float inv = 1.f / l_run;
+      const float l_row = aux_l[i] + aux_l[kRows + i];
+      const float inv = 1.f / l_row;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(tmem + lanes + kTmO + c * 32, o);
+        tc::tmem_ld32(tmem + lanes + kTmO + 128 * hh + 32 * c, o);
         tc::tmem_ld_wait();
         if (!rvalid) continue;
+        const int col = 256 * static_cast<int>(rank) + 128 * hh + 32 * c;
         if constexpr (kDecode) {
-          uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (slot0 + i) * kLatent + 256 * rank + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (slot0 + i) * kLatent + col);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * inv),
+                                __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
+                                __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
+                                __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o_lat) + qrow * kLatent + 256 * rank + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o_lat) + qrow * kLatent + col);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -314,152 +485,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) attn_tc
           }
         }
       }
-      if (rank == 0 && rvalid) {
+      if (rank == 0 && hh == 0 && rvalid) {
         if constexpr (kDecode) {
           a.ws_ml[2 * (slot0 + i)] = m_run;
-          a.ws_ml[2 * (slot0 + i) + 1] = l_run;
+          a.ws_ml[2 * (slot0 + i) + 1] = l_row;
         } else if (a.lse != nullptr) {
-          a.lse[qrow] = (m_run + log2f(l_run)) * kLn2;
+          a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
         }
       }
     }
-    if (!ok) B.abort = 1;
-  } else if (warp < 8) {
+  } else if (warp < kMmaWarp) {
     // ============================ producer =====================================
-    const int pt = threadIdx.x - 128;
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int st = j % kStages;
-      if (j >= kStages) ok = mbar_wait_bounded(&B.kv_empty[st], ((j / kStages) - 1) & 1, a.polls, a.err);
-      if (!ok) break;
-      uint8_t* stage = sKV + st * kKvStage;
-      const int k0 = j * kBK;
-      if constexpr (!kQ8) {
-        // units of 8 values: per key 32 latent units (+8 RoPE units on rank 0)
-        const int upk = nch * 8;
-        const int nu = kBK * upk / 128;                 // 20 or 16 per thread
-        uint4 v[20];
-#pragma unroll
-        for (int t = 0; t < 20; ++t) {
-          if (t < nu) {
-            const int idx = pt + t * 128;
-            const int key = idx / upk, cu = idx % upk;
-            const int dim = cu < 32 ? 256 * static_cast<int>(rank) + cu * 8 : kLatent + (cu - 32) * 8;
-            v[t] = make_uint4(0, 0, 0, 0);
-            if (k0 + key < kend)
-              v[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.kv) +
-                                                          (key_base + k0 + key) * kRow + dim));
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 20; ++t) {
-          if (t < nu) {
-            const int idx = pt + t * 128;
-            const int key = idx / upk, cu = idx % upk;
-            st_unit(stage + (cu >> 3) * kKvChunk, key, cu & 7, bf16x8_to_f16x8(v[t]));
-          }
-        }
-      } else {
-        // units of 16 codes: per key 16 latent units (+4 RoPE units on rank 0)
-        const int upk = nch * 4;
-        const int nu = kBK * upk / 128;                 // 10 or 8 per thread
-        uint4 v[10];
-        float d[10];
-#pragma unroll
-        for (int t = 0; t < 10; ++t) {
-          if (t < nu) {
-            const int idx = pt + t * 128;
-            const int key = idx / upk, cu = idx % upk;
-            const int dim = cu < 16 ? 256 * static_cast<int>(rank) + cu * 16 : kLatent + (cu - 16) * 16;
-            v[t] = make_uint4(0, 0, 0, 0);
-            d[t] = 0.f;
-            if (k0 + key < kend) {
-              const int64_t row = key_base + k0 + key;
-              v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
-              d[t] = __half2float(__ushort_as_half(__ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row)));
-            }
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 10; ++t) {
-          if (t < nu) {
-            const int idx = pt + t * 128;
-            const int key = idx / upk, cu = idx % upk;
-            const int c = cu >> 2, u = (cu & 3) * 2;    // chunk and first 8-element unit
-            uint4 lo, hi;
-            lo.x = i8x2_to_f16x2(v[t].x, 0, d[t]);  lo.y = i8x2_to_f16x2(v[t].x, 16, d[t]);
-            lo.z = i8x2_to_f16x2(v[t].y, 0, d[t]);  lo.w = i8x2_to_f16x2(v[t].y, 16, d[t]);
-            hi.x = i8x2_to_f16x2(v[t].z, 0, d[t]);  hi.y = i8x2_to_f16x2(v[t].z, 16, d[t]);
-            hi.z = i8x2_to_f16x2(v[t].w, 0, d[t]);  hi.w = i8x2_to_f16x2(v[t].w, 16, d[t]);
-            st_unit(stage + c * kKvChunk, key, u, lo);
-            st_unit(stage + c * kKvChunk, key, u + 1, hi);
-          }
-        }
-      }
-      tc::fence_proxy_async();
-      mbar_arrive(&B.kv_full[st]);
-    }
-    if (!ok) B.abort = 1;
+    const int pt = threadIdx.x - kSoftmaxWarps * 32;
+    if (rank == 0)
+      run_producer<kQ8, true>(&tm_rope, a, B, sLat, sRope, 0, pt, key_base, kend, n_tiles);
+    else
+      run_producer<kQ8, false>(&tm_rope, a, B, sLat, sRope, 1, pt, key_base, kend, n_tiles);
   } else if (lane == 0) {
     // ============================== MMA issue ==================================
-    constexpr uint32_t idesc_qk = tc::idesc_f16(128, kBK, false, false, false);
+    constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
+    constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kQ8, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
     bool ok = mbar_wait_bounded(&B.q_ready, 0, a.polls, a.err);
     tc::fence_after_sync();
-    auto issue_pv = [&](int jj) -> bool {
-      if (!mbar_wait_bounded(&B.p_full, jj & 1, a.polls, a.err)) return false;
+    auto issue_qk = [&](int t) -> bool {
+      const int ls = t % kLatStages, rs = t % kRopeStages, sb = t & 1;
+      if (!mbar_wait_bounded(&B.lat_full[ls], (t / kLatStages) & 1, a.polls, a.err)) return false;
+      if (!kQ8 && rank == 0 && !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.polls, a.err))
+        return false;
+      if (t >= 2 && !mbar_wait_bounded(&B.s_free[sb], ((t >> 1) - 1) & 1, a.polls, a.err)) return false;
       tc::fence_after_sync();
-      const uint32_t v0 = smem_u32(sKV + (jj % kStages) * kKvStage);
+      const uint32_t k0 = smem_u32(sLat + ls * kLatStage);
+      const uint32_t d = tmem + kTmS + sb * 64;
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks)        // latent half: A = Q from TMEM
+        tc::mma_ts(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024),
+                   idesc_lat, ks > 0 ? 1u : 0u);
+      if (rank == 0) {
+        const uint32_t q0 = smem_u32(sQr), r0 = smem_u32(sRope + rs * kChunk);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)       // RoPE part: A = Q_pe from smem
+          tc::mma_ss(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024), idesc_rope,
+                     1u);
+        tc::mma_commit(&B.rope_empty[rs]);
+      }
+      tc::mma_commit(&B.s_full[sb]);
+      return true;
+    };
+    auto issue_pv = [&](int t) -> bool {
+      if (!mbar_wait_bounded(&B.p_full, t & 1, a.polls, a.err)) return false;
+      tc::fence_after_sync();
+      const uint32_t v0 = smem_u32(sLat + (t % kLatStages) * kLatStage);
       const uint32_t p0 = smem_u32(sP);
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks)
         tc::mma_ss(tmem + kTmO, tc::sdesc_sw128(p0 + ks * 32, 16, 1024),
-                   tc::sdesc_sw128(v0 + ks * 2048, kKvChunk, 1024), idesc_pv, (jj > 0 || ks > 0) ? 1u : 0u);
-      tc::mma_commit(&B.kv_empty[jj % kStages]);
+                   tc::sdesc_sw128(v0 + ks * 2048, kChunk, 1024), idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+      tc::mma_commit(&B.lat_empty[t % kLatStages]);
       tc::mma_commit(&B.pv_done);
       return true;
     };
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int st = j % kStages, b = j & 1;
-      ok = mbar_wait_bounded(&B.kv_full[st], (j / kStages) & 1, a.polls, a.err);
-      if (ok && j >= 2) ok = mbar_wait_bounded(&B.s_free[b], ((j - 2) >> 1) & 1, a.polls, a.err);
-      if (!ok) break;
-      tc::fence_after_sync();
-      const uint32_t k0 = smem_u32(sKV + st * kKvStage);
-      const uint32_t d = tmem + kTmS + b * 64;
-#pragma unroll
-      for (int ks = 0; ks < 16; ++ks)        // latent half: A = Q from TMEM
-        tc::mma_ts(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kKvChunk + (ks & 3) * 32, 16, 1024),
-                   idesc_qk, ks > 0 ? 1u : 0u);
-      if (rank == 0) {
-        const uint32_t q0 = smem_u32(sQr);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)       // RoPE part: A = Q_pe from smem
-          tc::mma_ss(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024),
-                     tc::sdesc_sw128(k0 + 4 * kKvChunk + ks * 32, 16, 1024), idesc_qk, 1u);
-      }
-      tc::mma_commit(&B.s_full[b]);
-      if (j >= 1) ok = issue_pv(j - 1);
+    // Scores run three tiles ahead of P.V.
+    for (int t = 0; ok && t < 3 && t < n_tiles; ++t) ok = issue_qk(t);
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      ok = issue_pv(t);
+      if (ok && t + 3 < n_tiles) ok = issue_qk(t + 3);
     }
-    if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
-    if (!ok) B.abort = 1;
   }
 
   tc::fence_before_sync();
   __syncthreads();
   tc::cluster_sync();                 // no exchange may target a CTA that has left
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
 }
 
 template <bool kQ8, bool kDecode>
-cudaError_t launch_one(const AttnTcArgs& a, int n_items, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_items, cudaStream_t stream) {
   auto kern = attn_tc_kernel<kQ8, kDecode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(2 * n_items), kThreads, kSmem, stream>>>(a);
+  kern<<<dim3(2 * n_items), kThreads, kSmem, stream>>>(tm, a);
   return cudaGetLastError();
 }
 
@@ -469,8 +577,18 @@ int attn_tc_rows_per_item() { return kRows; }
 
 cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  if (q8) return decode ? launch_one<true, true>(a, n_items, stream) : launch_one<true, false>(a, n_items, stream);
-  return decode ? launch_one<false, true>(a, n_items, stream) : launch_one<false, false>(a, n_items, stream);
+  // Tensor map of the bf16 cache rows the kernel may address, for the RoPE
+  // tiles (64 keys x 64 dims, 128-byte swizzle); rows past n_rows read as zero.
+  CUtensorMap tm;
+  if (!q8) {
+    const uint64_t rows = static_cast<uint64_t>(a.n_rows);
+    cudaError_t e = make_tmap_3d(&tm, a.kv, true, kRow, rows, 1, kRow * 2, rows * kRow * 2, 64, kBK, 1);
+    if (e != cudaSuccess) return e;
+  } else {
+    memset(&tm, 0, sizeof(tm));
+  }
+  if (q8) return decode ? launch_one<true, true>(tm, a, n_items, stream) : launch_one<true, false>(tm, a, n_items, stream);
+  return decode ? launch_one<false, true>(tm, a, n_items, stream) : launch_one<false, false>(tm, a, n_items, stream);
 }
 
 }  // namespace mla

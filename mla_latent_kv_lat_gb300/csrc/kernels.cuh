@@ -1,6 +1,8 @@
 // Internal kernel interfaces of libmla (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace mla {
@@ -32,6 +34,7 @@ struct AttnTcArgs {
   const int8_t* kv_q;       // int8 [n_rows][576]
   const uint16_t* kv_d;     // fp16 [18][ld_d]
   int64_t ld_d;
+  int64_t n_rows;           // rows of the cache arrays the kernel may address
   int n_head;
   float scale_log2;         // softmax scale * log2(e)
   // prefill
@@ -44,11 +47,15 @@ struct AttnTcArgs {
   const int32_t* seq_len;
   int n_split;
   int chunk;
-  float* ws_o;              // fp32 [B * n_split][H][512]
-  float* ws_ml;             // fp32 [B * n_split][H][2]
+  float* ws_o;              // fp32 [B * n_split][H][512] partial o_lat, normalised by its own sum
+  float* ws_ml;             // fp32 [B * n_split][H][2]   running max (log2 units) and sum
   int* err;
   uint32_t polls;
 };
+
+// 3-D tiled tensor map of 16-bit elements with 128-byte swizzle (zero fill outside).
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
 cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream);
 int attn_tc_rows_per_item();

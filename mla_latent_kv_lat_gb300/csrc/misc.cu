@@ -58,8 +58,9 @@ cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t 
 }
 
 // ---------------------------------------------------------------------------
-// Split-KV combine: merge the per-split (m, l, o) of each (sequence, head) by
-// log-sum-exp and write o_lat in fp16.
+// Split-KV combine: merge the per-split partials of each (sequence, head) --
+// o_s normalised by its own sum l_s, running max m_s in log2 units -- by
+// log-sum-exp, and write o_lat in fp16.
 // ---------------------------------------------------------------------------
 namespace {
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
@@ -76,8 +77,9 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
   const int col = threadIdx.x * 4;
   for (int s = 0; s < ns; ++s) {
     const int64_t slot = (static_cast<int64_t>(b) * c.n_split + s) * c.n_head + h;
-    const float w = exp2f(c.ws_ml[2 * slot] - M);
-    L += w * c.ws_ml[2 * slot + 1];
+    // partials are normalised by their own sum l_s: weight 2^(m_s - M) * l_s
+    const float w = exp2f(c.ws_ml[2 * slot] - M) * c.ws_ml[2 * slot + 1];
+    L += w;
     const float4 o = *reinterpret_cast<const float4*>(c.ws_o + slot * kLatent + col);
     acc.x = fmaf(w, o.x, acc.x);
     acc.y = fmaf(w, o.y, acc.y);

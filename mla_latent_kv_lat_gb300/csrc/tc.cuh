@@ -172,5 +172,45 @@ MLA_DEVINL bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Arrive once on an mbarrier of another CTA of the cluster (release at
+// cluster scope: this thread's earlier memory accesses are ordered before).
+MLA_DEVINL void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// Named barrier over `nthreads` threads that also returns the OR of `pred`
+// over them.
+MLA_DEVINL bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred ip, op;\n\t"
+      "setp.ne.u32 ip, %2, 0;\n\t"
+      "bar.red.or.pred op, %1, %3, ip;\n\t"
+      "selp.u32 %0, 1, 0, op;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(pred ? 1u : 0u), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// fp32(h) + f: one fp16 operand (the low or high half of `w`) added in fp32.
+MLA_DEVINL float add_f16lo_f32(uint32_t w, float f) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}" : "=f"(r) : "r"(w), "f"(f));
+  return r;
+}
+MLA_DEVINL float add_f16hi_f32(uint32_t w, float f) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}" : "=f"(r) : "r"(w), "f"(f));
+  return r;
+}
+
+// 2^x with the hardware approximation (flushes subnormal results to zero).
+MLA_DEVINL float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace tc
 }  // namespace mla
