@@ -29,8 +29,9 @@
 //     tensor core reads.  The bf16 RoPE part arrives by TMA.
 //   * Roles per CTA: warps 0-7 softmax / exchange / epilogue (two threads per
 //     row, 32 keys of each 64-key tile each), warps 8-14 producer, warp 15 MMA
-//     issue.  Every wait is bounded; a failed wait is passed between the two
-//     warps that share rows so that both leave.
+//     issue.  Every mbarrier wait is bounded; the two softmax warps that share
+//     rows meet at a named barrier once per tile, and a warp whose wait gave up
+//     keeps meeting its partner (doing no other work) so that neither can hang.
 #include <string.h>
 
 #include "kernels.cuh"
@@ -79,7 +80,6 @@ struct Bars {
   uint64_t p_full;
   uint64_t pv_done;
   uint64_t q_ready;
-  uint64_t pair[4];          // the two softmax warps that share 32 rows, once per tile
   uint32_t tmem;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -270,7 +270,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&B.p_full, kSoftmaxWarps * 32);
     mbar_init(&B.pv_done, 1);
     mbar_init(&B.q_ready, kSoftmaxWarps * 32);
-    for (int i = 0; i < 4; ++i) mbar_init(&B.pair[i], 64);
     tc::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -329,14 +328,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer_x = tc::mapa(smem_u32(sX), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(&B.x_full[0]), peer);
     const uint32_t peer_xempty = tc::mapa(smem_u32(&B.x_empty[0]), peer);
+    const int bar_id = 1 + q4;                  // named barrier of the two warps sharing these rows
     float m_run = -INFINITY, l_h = 0.f;
-    bool ok = true;
+    // A wait that gave up makes the warp "dead": it skips every later wait,
+    // tensor-memory access and arrival, but still meets its partner warp at
+    // every named barrier, so neither warp of a pair can be left waiting.
+    bool dead = false;
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+      if (!dead) dead = !wait_all(bar, parity, a);
+    };
 
     // Read this thread's 32 partial scores of tile t, free the score buffer,
     // keep them as fp16 pairs and send the same pairs to the peer.
-    auto fetch_send = [&](int t, uint32_t (&own)[16]) -> bool {
+    auto fetch_send = [&](int t, uint32_t (&own)[16]) {
       const int sb = t & 1;
-      if (!wait_all(&B.s_full[sb], (t >> 1) & 1, a)) return false;
+      wait_ok(&B.s_full[sb], (t >> 1) & 1);
+      if (dead) return;
       tc::fence_after_sync();
       uint32_t r[32];
       tc::tmem_ld32(tmem + lanes + kTmS + sb * 64 + 32 * hh, r);
@@ -345,31 +352,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&B.s_free[sb]);
 #pragma unroll
       for (int k = 0; k < 16; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-      if (t >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1,
-                                                                           a.polls, a.err)))
-        return false;
+      if (t >= 2 && !dead)
+        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1, a.polls,
+                                                                      a.err));
+      if (dead) return;
 #pragma unroll
       for (int g = 0; g < 4; ++g)
         tc::st_async_v4(peer_x + sb * kXBytes + ((4 * hh + g) * kRows + i) * 16,
                         make_uint4(own[4 * g], own[4 * g + 1], own[4 * g + 2], own[4 * g + 3]), peer_xfull + sb * 8);
       if (threadIdx.x == 0) mbar_arrive_expect_tx(&B.x_full[sb], kXBytes);
-      return true;
     };
 
-    // Meet the partner warp (same rows, other key half) once per phase; a wait
-    // that gave up is passed on so that both warps leave together.
-    auto pair_sync = [&](int phase, bool ok_in) -> bool {
-      if (lane == 0) aux_fail[(phase & 1) * 8 + warp] = ok_in ? 0 : 1;
-      mbar_arrive(&B.pair[q4]);
-      const bool okp = wait_all(&B.pair[q4], phase & 1, a);
-      return okp && ok_in && aux_fail[(phase & 1) * 8 + partner] == 0;
+    // Meet the partner warp (same rows, other key half): publish `val` and this
+    // warp's state, return the partner's value.
+    auto pair_exchange = [&](float* slot_mine, const float* slot_theirs, float val, int phase) -> float {
+      *slot_mine = val;
+      if (lane == 0) aux_fail[(phase & 1) * 8 + warp] = dead ? 1 : 0;
+      tc::named_bar_sync(bar_id, 64);
+      if (aux_fail[(phase & 1) * 8 + partner] != 0) dead = true;
+      return *slot_theirs;
     };
 
     // Softmax of tile j from the two fp16 partials.
-    auto process = [&](int j, const uint32_t (&own)[16]) -> bool {
+    auto process = [&](int j, const uint32_t (&own)[16]) {
       const int xb = j & 1;
-      const bool okx =
-          __all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.polls, a.err));
+      if (!dead)
+        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.polls, a.err));
       float s[32];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -382,8 +390,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[8 * g + 2 * e + 1] = tc::add_f16hi_f32(pw[e], x.y);
         }
       }
-      __syncwarp();
-      if (okx && lane == 0) tc::mbar_arrive_remote(peer_xempty + xb * 8);   // this warp is done with buffer xb
       const int k0 = j * kBK + 32 * hh;
       if (k0 + 31 > lim) {
 #pragma unroll
@@ -394,9 +400,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 1; k < 32; ++k) mt = fmaxf(mt, s[k]);
       mt *= c2;
-      aux_m[((j & 1) * 2 + hh) * kRows + i] = mt;
-      if (!pair_sync(j, okx)) return false;
-      const float mrow = fmaxf(mt, aux_m[((j & 1) * 2 + (1 - hh)) * kRows + i]);
+      const float mo = pair_exchange(&aux_m[((j & 1) * 2 + hh) * kRows + i],
+                                     &aux_m[((j & 1) * 2 + (1 - hh)) * kRows + i], mt, j);
+      const float mrow = fmaxf(mt, mo);
       // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
       float alpha = 1.f;
       if (mrow > m_run + kRescaleThreshold) {
@@ -404,58 +410,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_run = mrow;
         l_h *= alpha;
       }
+      // p = 2^(s*c - m) on packed halves; the row sum stays in fp32.
       uint32_t pk[16];
       float lsum = 0.f;
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float p0 = tc::exp2_approx(fmaf(s[2 * k], c2, -m_run));
-        const float p1 = tc::exp2_approx(fmaf(s[2 * k + 1], c2, -m_run));
-        lsum += p0 + p1;
-        pk[k] = pack_f16x2(p0, p1);
+        pk[k] = tc::exp2_approx_f16x2(pack_f16x2(fmaf(s[2 * k], c2, -m_run), fmaf(s[2 * k + 1], c2, -m_run)));
+        lsum = tc::add_f16hi_f32(pk[k], tc::add_f16lo_f32(pk[k], lsum));
       }
       l_h += lsum;
       // P.V of tile j-1 has finished: the P buffer is free and O is stable.
       if (j >= 1) {
-        if (!wait_all(&B.pv_done, (j - 1) & 1, a)) return false;
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        wait_ok(&B.pv_done, (j - 1) & 1);
+        if (!dead) {
+          tc::fence_after_sync();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            const uint32_t col = tmem + lanes + kTmO + 128 * hh + 32 * c;
-            tc::tmem_ld32(col, o);
-            tc::tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              const uint32_t col = tmem + lanes + kTmO + 128 * hh + 32 * c;
+              tc::tmem_ld32(col, o);
+              tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st32(col, o);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::tmem_st32(col, o);
+            }
+            tc::tmem_st_wait();
           }
-          tc::tmem_st_wait();
         }
       }
+      if (dead) return;
 #pragma unroll
       for (int g = 0; g < 4; ++g)
         st_unit(sP, i, 4 * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
       tc::fence_proxy_async();
       tc::fence_before_sync();
       mbar_arrive(&B.p_full);
-      return true;
+      // This warp has long finished reading exchange buffer xb (every value read
+      // from it fed the scores above): tell the peer it may refill it.  A relaxed
+      // arrival suffices and avoids the ~1.4k-cycle cluster-scope release.
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_xempty + xb * 8);
     };
 
     uint32_t ownA[16], ownB[16];
-    ok = fetch_send(0, ownA);
-    for (int j = 0; ok && j < n_tiles; j += 2) {
-      if (j + 1 < n_tiles) ok = fetch_send(j + 1, ownB);
-      ok = ok && process(j, ownA);
-      if (!ok || j + 1 >= n_tiles) break;
-      if (j + 2 < n_tiles) ok = fetch_send(j + 2, ownA);
-      ok = ok && process(j + 1, ownB);
+    fetch_send(0, ownA);
+    for (int j = 0; j < n_tiles; j += 2) {
+      if (j + 1 < n_tiles) fetch_send(j + 1, ownB);
+      process(j, ownA);
+      if (j + 1 >= n_tiles) break;
+      if (j + 2 < n_tiles) fetch_send(j + 2, ownA);
+      process(j + 1, ownB);
     }
-    if (ok) ok = wait_all(&B.pv_done, (n_tiles - 1) & 1, a);
-    aux_l[hh * kRows + i] = l_h;
-    ok = pair_sync(n_tiles, ok);
-    if (ok) {
+    wait_ok(&B.pv_done, (n_tiles - 1) & 1);
+    const float l_other = pair_exchange(&aux_l[hh * kRows + i], &aux_l[(1 - hh) * kRows + i], l_h, n_tiles);
+    if (!dead) {
       tc::fence_after_sync();
-      const float l_row = aux_l[i] + aux_l[kRows + i];
+      const float l_row = hh == 0 ? l_h + l_other : l_other + l_h;
       const float inv = 1.f / l_row;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {

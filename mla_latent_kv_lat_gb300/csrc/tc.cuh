@@ -178,6 +178,14 @@ MLA_DEVINL void mbar_arrive_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
+// Arrive once on an mbarrier of another CTA of the cluster without ordering
+// earlier memory accesses.  For signalling "done reading": only use it after
+// every value read from the buffer has been consumed by later instructions,
+// so that those reads have completed when the arrival is issued.
+MLA_DEVINL void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
 // Named barrier over `nthreads` threads that also returns the OR of `pred`
 // over them.
 MLA_DEVINL bool bar_red_or(int id, int nthreads, bool pred) {
@@ -203,6 +211,13 @@ MLA_DEVINL float add_f16hi_f32(uint32_t w, float f) {
   float r;
   asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}" : "=f"(r) : "r"(w), "f"(f));
   return r;
+}
+
+// Two 2^x of packed halves with the hardware approximation.
+MLA_DEVINL uint32_t exp2_approx_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // 2^x with the hardware approximation (flushes subnormal results to zero).
