@@ -170,10 +170,14 @@ struct Producer {
   }
 };
 
+// kRope: this producer writes the RoPE ring (q8_0 cache, rank 0).  With a bf16
+// cache the RoPE tiles come by TMA, issued when `tma_rope` is set (rank 0).
 template <bool kQ8, bool kRope>
 MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Bars& B, uint8_t* sLat,
-                             uint8_t* sRope, int rank, int pt, int64_t key_base, int kend, int n_tiles) {
+                             uint8_t* sRope, int rank, bool tma_rope, int pt, int64_t key_base, int kend,
+                             int n_tiles) {
   using P = Producer<kQ8, kRope>;
+  const bool uses_rope = kRope || tma_rope;
   P x, y;
   // Tile j+1's loads are in flight while tile j is converted and stored.
   auto step = [&](int j, P& cur, P& nxt) -> bool {
@@ -181,11 +185,11 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
     const int ls = j % kLatStages, rs = j % kRopeStages;
     if (j >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((j / kLatStages) - 1) & 1, a.polls, a.err))
       return false;
-    if (kRope && j >= kRopeStages &&
+    if (uses_rope && j >= kRopeStages &&
         !mbar_wait_bounded(&B.rope_empty[rs], ((j / kRopeStages) - 1) & 1, a.polls, a.err))
       return false;
-    if constexpr (kRope && !kQ8) {            // bf16 RoPE keys by TMA, straight into the B-operand layout
-      if (pt == 0) {
+    if constexpr (!kQ8) {                     // bf16 RoPE keys by TMA, straight into the B-operand layout
+      if (tma_rope && pt == 0) {
         mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
         tc::tma_load_3d(sRope + rs * kChunk, tm_rope, &B.rope_full[rs], kLatent,
                         static_cast<int>(key_base + j * kBK), 0);
@@ -453,14 +457,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_xempty + xb * 8);
     };
 
-    uint32_t ownA[16], ownB[16];
-    fetch_send(0, ownA);
-    for (int j = 0; j < n_tiles; j += 2) {
-      if (j + 1 < n_tiles) fetch_send(j + 1, ownB);
-      process(j, ownA);
-      if (j + 1 >= n_tiles) break;
-      if (j + 2 < n_tiles) fetch_send(j + 2, ownA);
-      process(j + 1, ownB);
+    // One loop body (a register copy per tile keeps the hot code small).
+    uint32_t own[16], nxt[16];
+    fetch_send(0, own);
+#pragma unroll 1
+    for (int j = 0; j < n_tiles; ++j) {
+      if (j + 1 < n_tiles) fetch_send(j + 1, nxt);
+      process(j, own);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) own[k] = nxt[k];
     }
     wait_ok(&B.pv_done, (n_tiles - 1) & 1);
     const float l_other = pair_exchange(&aux_l[hh * kRows + i], &aux_l[(1 - hh) * kRows + i], l_h, n_tiles);
@@ -508,10 +513,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp < kMmaWarp) {
     // ============================ producer =====================================
     const int pt = threadIdx.x - kSoftmaxWarps * 32;
-    if (rank == 0)
-      run_producer<kQ8, true>(&tm_rope, a, B, sLat, sRope, 0, pt, key_base, kend, n_tiles);
-    else
-      run_producer<kQ8, false>(&tm_rope, a, B, sLat, sRope, 1, pt, key_base, kend, n_tiles);
+    if constexpr (kQ8) {
+      if (rank == 0)
+        run_producer<true, true>(&tm_rope, a, B, sLat, sRope, 0, false, pt, key_base, kend, n_tiles);
+      else
+        run_producer<true, false>(&tm_rope, a, B, sLat, sRope, 1, false, pt, key_base, kend, n_tiles);
+    } else {
+      run_producer<false, false>(&tm_rope, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, key_base,
+                                 kend, n_tiles);
+    }
   } else if (lane == 0) {
     // ============================== MMA issue ==================================
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
