@@ -400,10 +400,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 32; ++k)
           if (k0 + k > lim) s[k] = -INFINITY;
       }
-      float mt = s[0];
+      // Row maximum of this half as a tree (short dependency chain).
+      float mx[16];
 #pragma unroll
-      for (int k = 1; k < 32; ++k) mt = fmaxf(mt, s[k]);
-      mt *= c2;
+      for (int k = 0; k < 16; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
+      const float mt = mx[0] * c2;
       const float mo = pair_exchange(&aux_m[((j & 1) * 2 + hh) * kRows + i],
                                      &aux_m[((j & 1) * 2 + (1 - hh)) * kRows + i], mt, j);
       const float mrow = fmaxf(mt, mo);
@@ -416,13 +421,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // p = 2^(s*c - m) on packed halves; the row sum stays in fp32.
       uint32_t pk[16];
-      float lsum = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};        // four independent partial sums
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         pk[k] = tc::exp2_approx_f16x2(pack_f16x2(fmaf(s[2 * k], c2, -m_run), fmaf(s[2 * k + 1], c2, -m_run)));
-        lsum = tc::add_f16hi_f32(pk[k], tc::add_f16lo_f32(pk[k], lsum));
+        ls[k & 3] = tc::add_f16hi_f32(pk[k], tc::add_f16lo_f32(pk[k], ls[k & 3]));
       }
-      l_h += lsum;
+      l_h += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // P.V of tile j-1 has finished: the P buffer is free and O is stable.
       if (j >= 1) {
         wait_ok(&B.pv_done, (j - 1) & 1);
