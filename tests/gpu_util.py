@@ -2,6 +2,9 @@
 the error statistics the tolerances are written in."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -36,6 +39,10 @@ def err_stats(got: np.ndarray, ref: np.ndarray):
 def assert_tol(got, ref, tol, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     mx, mean = err_stats(got, ref)
+    log = os.environ.get("MLA_PARITY_LOG")
+    if log:                                   # optional record of every checked error, one JSON line each
+        with open(log, "a") as f:
+            f.write(json.dumps({"what": what, "max_rel": mx, "mean_rel": mean, "tol": list(tol)}) + "\n")
     assert mx <= tol[0] and mean <= tol[1], f"{what}: max-rel {mx:.3e} (<= {tol[0]}), mean-rel {mean:.3e} (<= {tol[1]})"
     return mx, mean
 
