@@ -37,8 +37,11 @@
  * - Return value: MLA_OK or a negative mla_status.  Nothing aborts, traps or
  *   prints.  A launch error reported by the CUDA runtime maps to MLA_ERR_CUDA.
  * - Kernels that wait on asynchronous copies or tensor-core work bound every
- *   wait.  A wait that runs out records MLA_ERR_TIMEOUT in a per-device error
- *   word, abandons its tile and returns; mla_get_device_error() reads it.
+ *   wait (0.5 s of the GPU's global timer).  A wait that runs out records
+ *   MLA_ERR_TIMEOUT in a per-device error word, abandons its tile and
+ *   returns; mla_get_device_error() reads and clears it.  While the word is
+ *   set, any wait that does not complete at once gives up too, so a failing
+ *   launch (and any launch after it, until the word is read) ends quickly.
  * - Dims other than kv_lora_rank 512, qk_rope 64, qk_nope 128, v_head 128,
  *   or n_head not a multiple of 16 in [16, 128], return MLA_ERR_UNSUPPORTED.
  *
@@ -196,12 +199,12 @@ int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n,
 int mla_get_device_error(void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an
- * mbarrier phase nothing completes, giving up after `spins` polls (1 <= spins
- * <= 1<<20).  It records MLA_ERR_TIMEOUT in the device error word exactly as
+ * mbarrier phase nothing completes, giving up after `limit_us` microseconds
+ * (1 <= limit_us <= 1<<20).  It records MLA_ERR_TIMEOUT in the device error word exactly as
  * a kernel's real waits do, and returns normally.  No counterpart on the
  * pages: it exists so that tests can check failure reporting without
  * hanging or faulting a GPU.                                                  */
-int mla_selftest_wait_timeout(int32_t spins, void* stream);
+int mla_selftest_wait_timeout(int32_t limit_us, void* stream);
 
 /* Static description of a status code (never NULL).                           */
 const char* mla_status_string(int status);

@@ -213,8 +213,8 @@ def mla_get_device_error(stream=None) -> int:
     return int(load_library().mla_get_device_error(_stream(stream)))
 
 
-def mla_selftest_wait_timeout(spins: int, stream=None):
-    _check("mla_selftest_wait_timeout", load_library().mla_selftest_wait_timeout(spins, _stream(stream)))
+def mla_selftest_wait_timeout(limit_us: int, stream=None):
+    _check("mla_selftest_wait_timeout", load_library().mla_selftest_wait_timeout(limit_us, _stream(stream)))
 
 
 def mla_status_string(status: int) -> str:

@@ -99,7 +99,7 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   a.o_lat = o_lat;
   a.lse = lse;
   a.err = err;
-  a.polls = kDefaultWaitPolls;
+  a.wait_us = kDefaultWaitUs;
   const int64_t items = (a.n_qrows + attn_tc_rows_per_item() - 1) / attn_tc_rows_per_item();
   if (items > (1 << 30)) return MLA_ERR_UNSUPPORTED;
   return to_status(launch_attn_tc(a, q8, false, static_cast<int>(items), static_cast<cudaStream_t>(stream)));
@@ -144,7 +144,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.ws_o = static_cast<float*>(workspace);
   a.ws_ml = a.ws_o + slots * kLatent;
   a.err = err;
-  a.polls = kDefaultWaitPolls;
+  a.wait_us = kDefaultWaitUs;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = launch_attn_tc(a, q8, true, B * plan.n_split, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
@@ -170,7 +170,7 @@ int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32
   int* err = nullptr;
   if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
   HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, f32 ? 1 : 0};
-  return to_status(launch_head_gemm_tc(g, err, kDefaultWaitPolls, static_cast<cudaStream_t>(stream)));
+  return to_status(launch_head_gemm_tc(g, err, kDefaultWaitUs, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -243,11 +243,11 @@ int mla_get_device_error(void* stream) {
   return v;
 }
 
-int mla_selftest_wait_timeout(int32_t spins, void* stream) {
-  if (spins < 1 || spins > (1 << 20)) return MLA_ERR_INVALID_ARG;
+int mla_selftest_wait_timeout(int32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > (1 << 20)) return MLA_ERR_INVALID_ARG;
   int* err = nullptr;
   if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
-  return to_status(launch_wait_timeout_selftest(static_cast<uint32_t>(spins), err,
+  return to_status(launch_wait_timeout_selftest(static_cast<uint32_t>(limit_us), err,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

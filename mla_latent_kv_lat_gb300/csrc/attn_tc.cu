@@ -86,7 +86,7 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 static_assert(kSmem <= 232448, "shared memory");
 
 MLA_DEVINL bool wait_all(uint64_t* bar, uint32_t parity, const AttnTcArgs& a) {
-  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.polls, a.err));
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.wait_us, a.err));
 }
 
 // Store one 16-byte unit (8 halves) into a 128-byte-swizzled K-major tile.
@@ -183,10 +183,10 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   auto step = [&](int j, P& cur, P& nxt) -> bool {
     if (j + 1 < n_tiles) nxt.load(a, rank, pt, key_base, (j + 1) * kBK, kend);
     const int ls = j % kLatStages, rs = j % kRopeStages;
-    if (j >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((j / kLatStages) - 1) & 1, a.polls, a.err))
+    if (j >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((j / kLatStages) - 1) & 1, a.wait_us, a.err))
       return false;
     if (uses_rope && j >= kRopeStages &&
-        !mbar_wait_bounded(&B.rope_empty[rs], ((j / kRopeStages) - 1) & 1, a.polls, a.err))
+        !mbar_wait_bounded(&B.rope_empty[rs], ((j / kRopeStages) - 1) & 1, a.wait_us, a.err))
       return false;
     if constexpr (!kQ8) {                     // bf16 RoPE keys by TMA, straight into the B-operand layout
       if (tma_rope && pt == 0) {
@@ -357,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 16; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
       if (t >= 2 && !dead)
-        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1, a.polls,
+        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1, a.wait_us,
                                                                       a.err));
       if (dead) return;
 #pragma unroll
@@ -381,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto process = [&](int j, const uint32_t (&own)[16]) {
       const int xb = j & 1;
       if (!dead)
-        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.polls, a.err));
+        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.wait_us, a.err));
       float s[32];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -532,14 +532,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
     constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kQ8, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
-    bool ok = mbar_wait_bounded(&B.q_ready, 0, a.polls, a.err);
+    bool ok = mbar_wait_bounded(&B.q_ready, 0, a.wait_us, a.err);
     tc::fence_after_sync();
     auto issue_qk = [&](int t) -> bool {
       const int ls = t % kLatStages, rs = t % kRopeStages, sb = t & 1;
-      if (!mbar_wait_bounded(&B.lat_full[ls], (t / kLatStages) & 1, a.polls, a.err)) return false;
-      if (!kQ8 && rank == 0 && !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.polls, a.err))
+      if (!mbar_wait_bounded(&B.lat_full[ls], (t / kLatStages) & 1, a.wait_us, a.err)) return false;
+      if (!kQ8 && rank == 0 && !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.wait_us, a.err))
         return false;
-      if (t >= 2 && !mbar_wait_bounded(&B.s_free[sb], ((t >> 1) - 1) & 1, a.polls, a.err)) return false;
+      if (t >= 2 && !mbar_wait_bounded(&B.s_free[sb], ((t >> 1) - 1) & 1, a.wait_us, a.err)) return false;
       tc::fence_after_sync();
       const uint32_t k0 = smem_u32(sLat + ls * kLatStage);
       const uint32_t d = tmem + kTmS + sb * 64;
@@ -559,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return true;
     };
     auto issue_pv = [&](int t) -> bool {
-      if (!mbar_wait_bounded(&B.p_full, t & 1, a.polls, a.err)) return false;
+      if (!mbar_wait_bounded(&B.p_full, t & 1, a.wait_us, a.err)) return false;
       tc::fence_after_sync();
       const uint32_t v0 = smem_u32(sLat + (t % kLatStages) * kLatStage);
       const uint32_t p0 = smem_u32(sP);

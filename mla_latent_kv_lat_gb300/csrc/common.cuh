@@ -21,10 +21,13 @@ constexpr int kVHead = 128;    // v_head
 constexpr int kQ8Block = 32;   // q8_0 block size
 constexpr int kQ8Blocks = kRow / kQ8Block;   // 18 blocks per row
 
-// Default number of polls before a bounded wait gives up.  A poll is one
-// mbarrier.try_wait, which itself suspends for a hardware-defined time, so
-// this bounds a stuck wait to well under a second on GB300.
-constexpr uint32_t kDefaultWaitPolls = 1u << 22;
+// Time after which a bounded wait gives up, in microseconds of %globaltimer.
+// Every wait inside a kernel normally completes within microseconds.
+constexpr uint32_t kDefaultWaitUs = 500000;
+// Longest time one try_wait may keep a waiting thread suspended.  The thread
+// wakes as soon as the phase completes, so this only sets how often a stuck
+// wait re-checks its time limit.
+constexpr uint32_t kWaitSuspendNs = 20000;
 
 // Record the first device-side error; later errors keep the first one.
 MLA_DEVINL void record_error(int* err, int code) {
@@ -106,14 +109,53 @@ MLA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for phase `parity` of `bar` to complete.  Returns false (and
-// records MLA_ERR_TIMEOUT) if it did not complete within `polls` polls.
-MLA_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t polls, int* err) {
-  for (uint32_t i = 0; i < polls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+// try_wait that lets the hardware suspend the thread for up to `ns`
+// nanoseconds (or until the phase completes) instead of returning at once.
+// A waiting warp then takes no issue slots from the warps doing the work.
+MLA_DEVINL bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+MLA_DEVINL uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// The slow path shared by the bounded waits: keep trying (suspended between
+// tries) until `done()` holds, `limit_us` microseconds have passed (records
+// MLA_ERR_TIMEOUT) or another thread has already recorded an error, in which
+// case the launch is failing anyway and this wait gives up at once, so that a
+// failed launch ends quickly instead of each CTA timing out in turn.  While
+// the error word is set (until the host reads it), a wait that does not
+// complete at once gives up.
+template <typename Done>
+MLA_DEVINL bool wait_slow(Done done, uint32_t limit_us, int* err) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (done()) return true;
+    if (err != nullptr && *reinterpret_cast<volatile int*>(err) != 0) return false;
+    if (global_timer_ns() - t0 > static_cast<uint64_t>(limit_us) * 1000u) {
+      record_error(err, MLA_ERR_TIMEOUT);
+      return false;
+    }
   }
-  record_error(err, MLA_ERR_TIMEOUT);
-  return false;
+}
+
+// Bounded wait for phase `parity` of `bar` to complete.  Returns false if it
+// did not complete within `limit_us` microseconds (MLA_ERR_TIMEOUT recorded)
+// or an error was already recorded.
+MLA_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit_us, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow([&] { return mbar_try_wait_suspend(bar, parity, kWaitSuspendNs); }, limit_us, err);
 }
 
 }  // namespace mla

@@ -38,7 +38,7 @@ struct TcGemmArgs {
   const uint16_t* w;     // bf16 [H][K][N], read directly when converting to fp16
   int T, H, tiles;
   int* err;
-  uint32_t polls;
+  uint32_t wait_us;
 };
 
 template <int K, int N, int NSUB, bool kAbsorb>
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tt = grp + i * G;
         for (int kc = 0; kc < C::KC; ++kc) {
           const int u = i * C::KC + kc, st = u % kStages;
-          if (u >= kStages && !mbar_wait_bounded(&a_empty[st], ((u / kStages) - 1) & 1, g.polls, g.err)) {
+          if (u >= kStages && !mbar_wait_bounded(&a_empty[st], ((u / kStages) - 1) & 1, g.wait_us, g.err)) {
             abort_flag = 1;
             break;
           }
@@ -108,17 +108,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(w_full, 0, g.polls, g.err);
+      bool ok = mbar_wait_bounded(w_full, 0, g.wait_us, g.err);
       tc::fence_after_sync();
       constexpr uint32_t idesc = tc::idesc_f16(128, NSUB, kAbsorb, false, true);
       for (int i = 0; ok && i < n_tiles; ++i) {
         for (int j = 0; ok && j < C::NS; ++j) {
           const int job = i * C::NS + j, slot = job % C::SLOTS;
-          if (job >= C::SLOTS) ok = mbar_wait_bounded(&acc_empty[slot], ((job / C::SLOTS) - 1) & 1, g.polls, g.err);
+          if (job >= C::SLOTS) ok = mbar_wait_bounded(&acc_empty[slot], ((job / C::SLOTS) - 1) & 1, g.wait_us, g.err);
           tc::fence_after_sync();
           for (int kc = 0; ok && kc < C::KC; ++kc) {
             const int u = i * C::KC + kc, st = u % kStages;
-            if (j == 0) ok = mbar_wait_bounded(&a_full[st], (u / kStages) & 1, g.polls, g.err);
+            if (j == 0) ok = mbar_wait_bounded(&a_full[st], (u / kStages) & 1, g.wait_us, g.err);
             if (!ok) break;
             tc::fence_after_sync();
             const uint32_t a0 = smem_u32(sA + st * kChunkBytes);
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = tt * 128 + q * 32 + lane;
       for (int j = 0; ok && j < C::NS; ++j) {
         const int job = i * C::NS + j, slot = job % C::SLOTS;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[slot], (job / C::SLOTS) & 1, g.polls, g.err));
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[slot], (job / C::SLOTS) & 1, g.wait_us, g.err));
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
@@ -252,7 +252,7 @@ int device_sm_count() {
 }
 
 template <int K, int N, int NSUB, bool kAbsorb>
-static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cudaStream_t stream) {
+static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream) {
   using C = GemmCfg<K, N, NSUB>;
   CUtensorMap tmA, tmW;
   const uint64_t H = static_cast<uint64_t>(g.H);
@@ -271,7 +271,7 @@ static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cu
   a.H = g.H;
   a.tiles = (g.T + 127) / 128;
   a.err = err;
-  a.polls = polls;
+  a.wait_us = wait_us;
   const int sms = device_sm_count();
   int G = sms / g.H;
   if (G < 1) G = 1;
@@ -283,11 +283,11 @@ static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cu
   return cudaGetLastError();
 }
 
-cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cudaStream_t stream) {
+cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream) {
   if (g.K == kNope && g.N == kLatent && !g.out_f32 && !g.a_f16)
-    return launch_tc<kNope, kLatent, 256, true>(g, err, polls, stream);
+    return launch_tc<kNope, kLatent, 256, true>(g, err, wait_us, stream);
   if (g.K == kLatent && g.N == kVHead && g.out_f32 && g.a_f16)
-    return launch_tc<kLatent, kVHead, 128, false>(g, err, polls, stream);
+    return launch_tc<kLatent, kVHead, 128, false>(g, err, wait_us, stream);
   return cudaErrorInvalidValue;
 }
 

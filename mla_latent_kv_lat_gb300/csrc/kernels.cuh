@@ -50,7 +50,7 @@ struct AttnTcArgs {
   float* ws_o;              // fp32 [B * n_split][H][512] partial o_lat, normalised by its own sum
   float* ws_ml;             // fp32 [B * n_split][H][2]   running max (log2 units) and sum
   int* err;
-  uint32_t polls;
+  uint32_t wait_us;
 };
 
 // 3-D tiled tensor map of 16-bit elements with 128-byte swizzle (zero fill outside).
@@ -61,10 +61,10 @@ cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_item
 int attn_tc_rows_per_item();
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
-cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t polls, cudaStream_t stream);
+cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream);
 int device_sm_count();
 cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d,
                                  cudaStream_t stream);
-cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(uint32_t wait_us, int* err, cudaStream_t stream);
 
 }  // namespace mla

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const uint16_t* kv, 
   if (lane == 0) kv_d[static_cast<int64_t>(blk) * ld_d + row] = __float2half_rn(d);
 }
 
-__global__ void wait_timeout_selftest_kernel(uint32_t polls, int* err) {
+__global__ void wait_timeout_selftest_kernel(uint32_t wait_us, int* err) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -37,7 +37,7 @@ __global__ void wait_timeout_selftest_kernel(uint32_t polls, int* err) {
   }
   __syncthreads();
   // Nothing ever arrives on `bar`: phase 0 never completes.
-  if (threadIdx.x == 0) (void)mbar_wait_bounded(&bar, 0, polls, err);
+  if (threadIdx.x == 0) (void)mbar_wait_bounded(&bar, 0, wait_us, err);
   __syncthreads();
 }
 
@@ -52,8 +52,8 @@ cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_wait_timeout_selftest(uint32_t polls, int* err, cudaStream_t stream) {
-  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(polls, err);
+cudaError_t launch_wait_timeout_selftest(uint32_t wait_us, int* err, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(wait_us, err);
   return cudaGetLastError();
 }
 

@@ -165,11 +165,21 @@ MLA_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-MLA_DEVINL bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32_t polls, int* err) {
-  for (uint32_t i = 0; i < polls; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  record_error(err, MLA_ERR_TIMEOUT);
-  return false;
+MLA_DEVINL bool mbar_try_wait_cluster_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait_bounded with cluster-scope acquire (arrivals from the peer CTA).
+MLA_DEVINL bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32_t limit_us, int* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return wait_slow([&] { return mbar_try_wait_cluster_suspend(bar, parity, kWaitSuspendNs); }, limit_us, err);
 }
 
 // Arrive once on an mbarrier of another CTA of the cluster (release at
