@@ -180,7 +180,7 @@ def setup_workload(name, torch):
             mla.mla_late_decompress(bufs.o_lat, d["wv_b"], bufs.o, stream=stream)
         launches = 4
     else:
-        bufs = P.prefill_buffers(wl.T, wl.n_head)
+        bufs = P.prefill_buffers(wl.T, wl.n_head, n_kv=x.n_rows)
 
         def step(stream=None, ev=None):
             mla.mla_absorb_q(d["q_nope"], d["wk_b"], bufs.q_lat, stream=stream)
@@ -188,13 +188,14 @@ def setup_workload(name, torch):
                 ev[0].record()
             if wl.cache == "q8_0":
                 mla.mla_attn_prefill_q8_0(bufs.q_lat, d["q_pe"], d["kv_q"], d["kv_d"], wl.q_pos0, bufs.o_lat,
-                                          stream=stream)
+                                          stream=stream, workspace=bufs.workspace)
             else:
-                mla.mla_attn_prefill(bufs.q_lat, d["q_pe"], d["kv"], wl.q_pos0, bufs.o_lat, stream=stream)
+                mla.mla_attn_prefill(bufs.q_lat, d["q_pe"], d["kv"], wl.q_pos0, bufs.o_lat, stream=stream,
+                                     workspace=bufs.workspace)
             if ev:
                 ev[1].record()
             mla.mla_late_decompress(bufs.o_lat, d["wv_b"], bufs.o, stream=stream)
-        launches = 3
+        launches = 4    # absorb, fp16 cache staging, attention, late decompression
     return wl, x, d, bufs, step, launches
 
 

@@ -96,6 +96,11 @@ typedef enum mla_status {
 int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b,
                  void* q_lat, int32_t T, void* stream);
 
+/* Bytes of device workspace mla_attn_prefill / mla_attn_prefill_q8_0 need for
+ * a cache of n_kv rows: an fp16 copy of the rows a prefill reads (1152 bytes
+ * a row, rounded up to 256).  Returns 0 for invalid arguments.               */
+size_t mla_prefill_workspace_size(const mla_dims* dims, int32_t n_kv);
+
 /* Steps 2-4 for a causal prefill chunk (method page sec. 4, 5, 8.1):
  *   s[t][h][j] = scale * (q_pe[t][h] . k_pe[j] + q_lat[t][h] . c_kv[j])
  *   visible iff j <= q_pos0 + t   (query t sits at position q_pos0 + t)
@@ -103,13 +108,19 @@ int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b,
  * q_lat   device fp16 [T][H][512]
  * q_pe    device bf16 [T][H][64]
  * kv      device bf16 [n_kv][576]    latent cache (layout above)
+ * workspace device, ws_bytes >= mla_prefill_workspace_size(dims, n_kv): the
+ *         call first writes the rows it reads there as fp16 (every query
+ *         tile reads every visible row, so they are converted once, not once
+ *         per tile); its contents need not be kept between calls.
  * o_lat   device fp16 [T][H][512]    output
  * lse     device fp32 [T][H] or NULL; natural-log sum_j exp(s[t][h][j])
  * Requires T >= 1, q_pos0 >= 0 and q_pos0 + T <= n_kv.  Rows past
- * q_pos0 + T - 1 are never read.                                              */
+ * q_pos0 + T - 1 are never read.  MLA_ERR_WORKSPACE if the workspace is
+ * missing or too small.                                                       */
 int mla_attn_prefill(const mla_dims* dims, const void* q_lat, const void* q_pe,
                      const void* kv, int32_t n_kv, int32_t T, int32_t q_pos0,
-                     void* o_lat, float* lse, void* stream);
+                     void* workspace, size_t ws_bytes, void* o_lat, float* lse,
+                     void* stream);
 
 /* As mla_attn_prefill over a q8_0 latent cache (method page sec. 8.1):
  * kv_q device int8 [n_kv][576], kv_d device fp16 [18][n_kv].  Each block is
@@ -117,8 +128,8 @@ int mla_attn_prefill(const mla_dims* dims, const void* q_lat, const void* q_pe,
  * latent weighted sum.                                                        */
 int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe,
                           const int8_t* kv_q, const uint16_t* kv_d, int32_t n_kv,
-                          int32_t T, int32_t q_pos0, void* o_lat, float* lse,
-                          void* stream);
+                          int32_t T, int32_t q_pos0, void* workspace, size_t ws_bytes,
+                          void* o_lat, float* lse, void* stream);
 
 /* Bytes of device workspace mla_attn_decode / mla_attn_decode_q8_0 need for
  * B sequences no longer than max_len (split-KV partial results).  Returns 0

@@ -47,8 +47,9 @@ _D = ctypes.POINTER(MLADims)
 
 _SIGS = {
     "mla_absorb_q": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
-    "mla_attn_prefill": ([_D, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
-    "mla_attn_prefill_q8_0": ([_D, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "mla_prefill_workspace_size": ([_D, _I32], _SZ),
+    "mla_attn_prefill": ([_D, _P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P, _P], ctypes.c_int),
+    "mla_attn_prefill_q8_0": ([_D, _P, _P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P, _P], ctypes.c_int),
     "mla_decode_workspace_size": ([_D, _I32, _I32], _SZ),
     "mla_attn_decode": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "mla_attn_decode_q8_0": ([_D, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
@@ -130,27 +131,42 @@ def mla_late_decompress(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor
     _check("mla_late_decompress", load_library().mla_late_decompress(ctypes.byref(d), *args, T, _stream(stream)))
 
 
-def mla_attn_prefill(q_lat, q_pe, kv, q_pos0: int, o_lat, lse=None, scale=None, stream=None):
+def mla_prefill_workspace_size(n_head: int, n_kv: int, scale=None) -> int:
+    d = make_dims(n_head, scale)
+    return int(load_library().mla_prefill_workspace_size(ctypes.byref(d), n_kv))
+
+
+def _prefill_ws(workspace, H: int, n_kv: int, device):
+    """The caller's workspace, or a fresh one from PyTorch's allocator."""
+    if workspace is None:
+        workspace = torch.empty(mla_prefill_workspace_size(H, n_kv), dtype=torch.uint8, device=device)
+    return _need(workspace, "workspace", torch.uint8), workspace.numel()
+
+
+def mla_attn_prefill(q_lat, q_pe, kv, q_pos0: int, o_lat, lse=None, scale=None, stream=None, workspace=None):
     T, H = q_lat.shape[0], q_lat.shape[1]
     n_kv = kv.shape[0]
     d = make_dims(H, scale)
     lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
+    wp, wn = _prefill_ws(workspace, H, n_kv, kv.device)
     st = load_library().mla_attn_prefill(
         ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (T, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv, "kv", torch.bfloat16, (n_kv, ROW)),
-        n_kv, T, q_pos0, _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
+        n_kv, T, q_pos0, wp, wn, _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
     _check("mla_attn_prefill", st)
 
 
-def mla_attn_prefill_q8_0(q_lat, q_pe, kv_q, kv_d, q_pos0: int, o_lat, lse=None, scale=None, stream=None):
+def mla_attn_prefill_q8_0(q_lat, q_pe, kv_q, kv_d, q_pos0: int, o_lat, lse=None, scale=None, stream=None,
+                          workspace=None):
     T, H = q_lat.shape[0], q_lat.shape[1]
     n_kv = kv_q.shape[0]
     d = make_dims(H, scale)
     lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
+    wp, wn = _prefill_ws(workspace, H, n_kv, kv_q.device)
     st = load_library().mla_attn_prefill_q8_0(
         ctypes.byref(d), _need(q_lat, "q_lat", torch.float16, (T, H, KV_LORA_RANK)),
         _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv_q, "kv_q", torch.int8, (n_kv, ROW)),
-        _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_kv)), n_kv, T, q_pos0,
+        _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_kv)), n_kv, T, q_pos0, wp, wn,
         _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
     _check("mla_attn_prefill_q8_0", st)
 

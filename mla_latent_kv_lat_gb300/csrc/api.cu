@@ -71,9 +71,14 @@ size_t decode_ws_bytes(int H, int32_t B, int32_t max_len) {
   return slots * kLatent * sizeof(float) + slots * 2 * sizeof(float);
 }
 
+size_t prefill_ws_bytes(int32_t n_kv) {
+  // fp16 staging copy of the cache rows, rounded up to whole 256-byte lines
+  return (static_cast<size_t>(n_kv) * kRow * 2 + 255) & ~static_cast<size_t>(255);
+}
+
 int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv,
                    const int8_t* kv_q, const uint16_t* kv_d, int32_t n_kv, int32_t T, int32_t q_pos0,
-                   void* o_lat, float* lse, void* stream, bool q8) {
+                   void* workspace, size_t ws_bytes, void* o_lat, float* lse, void* stream, bool q8) {
   int s = check_dims(dims);
   if (s != MLA_OK) return s;
   s = q8 ? check_ptrs({q_lat, q_pe, kv_q, kv_d, o_lat}) : check_ptrs({q_lat, q_pe, kv, o_lat});
@@ -81,17 +86,21 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   if (lse != nullptr && !aligned16(lse)) return MLA_ERR_MISALIGNED;
   if (T < 1 || q_pos0 < 0 || n_kv < 1) return MLA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(q_pos0) + T > n_kv) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < prefill_ws_bytes(n_kv)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_MISALIGNED;
   int* err = nullptr;
   cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(q_pos0) + T;     // rows past the last query are never read
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = launch_stage_cache_f16(q8 ? nullptr : kv, kv_q, kv_d, n_kv, rows, workspace, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   AttnTcArgs a = {};
   a.q_lat = q_lat;
   a.q_pe = q_pe;
-  a.kv = kv;
-  a.kv_q = kv_q;
-  a.kv_d = kv_d;
+  a.kv = workspace;
   a.ld_d = n_kv;
-  a.n_rows = static_cast<int64_t>(q_pos0) + T;     // rows past the last query are never read
+  a.n_rows = rows;
   a.n_head = dims->n_head;
   a.scale_log2 = dims->scale * kLog2eF;
   a.q_pos0 = q_pos0;
@@ -102,7 +111,7 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   a.wait_us = kDefaultWaitUs;
   const int64_t items = (a.n_qrows + attn_tc_rows_per_item() - 1) / attn_tc_rows_per_item();
   if (items > (1 << 30)) return MLA_ERR_UNSUPPORTED;
-  return to_status(launch_attn_tc(a, q8, false, static_cast<int>(items), static_cast<cudaStream_t>(stream)));
+  return to_status(launch_attn_tc(a, false, false, static_cast<int>(items), st));
 }
 
 int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, const int8_t* kv_q,
@@ -190,15 +199,23 @@ int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_
   return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, true, stream);
 }
 
+size_t mla_prefill_workspace_size(const mla_dims* dims, int32_t n_kv) {
+  if (check_dims(dims) != MLA_OK || n_kv < 1) return 0;
+  return prefill_ws_bytes(n_kv);
+}
+
 int mla_attn_prefill(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, int32_t n_kv,
-                     int32_t T, int32_t q_pos0, void* o_lat, float* lse, void* stream) {
-  return prefill_common(dims, q_lat, q_pe, kv, nullptr, nullptr, n_kv, T, q_pos0, o_lat, lse, stream, false);
+                     int32_t T, int32_t q_pos0, void* workspace, size_t ws_bytes, void* o_lat, float* lse,
+                     void* stream) {
+  return prefill_common(dims, q_lat, q_pe, kv, nullptr, nullptr, n_kv, T, q_pos0, workspace, ws_bytes, o_lat, lse,
+                        stream, false);
 }
 
 int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q_pe, const int8_t* kv_q,
-                          const uint16_t* kv_d, int32_t n_kv, int32_t T, int32_t q_pos0, void* o_lat,
-                          float* lse, void* stream) {
-  return prefill_common(dims, q_lat, q_pe, nullptr, kv_q, kv_d, n_kv, T, q_pos0, o_lat, lse, stream, true);
+                          const uint16_t* kv_d, int32_t n_kv, int32_t T, int32_t q_pos0, void* workspace,
+                          size_t ws_bytes, void* o_lat, float* lse, void* stream) {
+  return prefill_common(dims, q_lat, q_pe, nullptr, kv_q, kv_d, n_kv, T, q_pos0, workspace, ws_bytes, o_lat, lse,
+                        stream, true);
 }
 
 size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_len) {

@@ -23,13 +23,16 @@
 //     the score MMAs overlap the softmax.
 //   * P (fp16) goes to shared memory; O_r += P V_r runs on tcgen05 with V_r read
 //     in place from the latent cache tile (MN-major view).
-//   * Latent cache tiles are loaded by seven producer warps with
-//     software-pipelined 16-byte loads, converted to fp16 (bf16: exact; q8_0:
-//     fp16 scale x int8 code) and stored in the 128-byte-swizzled layout the
-//     tensor core reads.  The bf16 RoPE part arrives by TMA.
+//   * Cache tiles.  Prefill: every cluster reads every visible cache row, so
+//     the rows are staged once as fp16 (latent and RoPE parts) before the
+//     kernel, and one thread brings each tile in by TMA, already in the
+//     128-byte-swizzled layout the tensor core reads.  Decode reads each row
+//     once: seven producer warps load the latent tiles with software-pipelined
+//     16-byte loads, convert them to fp16 (bf16: exact; q8_0: fp16 scale x
+//     int8 code) and store them swizzled; the bf16 RoPE part arrives by TMA.
 //   * Roles per CTA: warps 0-7 softmax / exchange / epilogue (two threads per
-//     row, 32 keys of each 64-key tile each), warps 8-14 producer, warp 15 MMA
-//     issue.  Every mbarrier wait is bounded; the two softmax warps that share
+//     row, 32 keys of each 64-key tile each); then the loader (prefill: one
+//     TMA warp; decode: seven producer warps); the last warp issues the MMAs.  Every mbarrier wait is bounded; the two softmax warps that share
 //     rows meet at a named barrier once per tile, and a warp whose wait gave up
 //     keeps meeting its partner (doing no other work) so that neither can hang.
 #include <string.h>
@@ -59,9 +62,11 @@ constexpr int kAuxBytes = (4 * kRows + 2 * kRows) * 4 + 16 * 4;
 constexpr int kOffBar = kOffAux + kAuxBytes;
 constexpr int kSmem = 1024 + kOffBar + 256;
 constexpr int kSoftmaxWarps = 8, kProducerWarps = 7;
-constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;   // 512: four warps per SM sub-partition
 constexpr int kProducerThreads = kProducerWarps * 32;
+// Loader warps: one TMA warp (prefill) or the producers (decode).
+__host__ __device__ constexpr int loader_warps(bool decode) { return decode ? kProducerWarps : 1; }
+__host__ __device__ constexpr int mma_warp(bool decode) { return kSoftmaxWarps + loader_warps(decode); }
+__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + 1) * 32; }   // decode 512, prefill 320
 // TMEM columns: Q latent half (A operand, 256 fp16 = 128 cols), two fp32 score
 // buffers of 64 columns, the fp32 output half (256 cols).
 constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 256;
@@ -210,9 +215,13 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// kDecode = false: prefill from the fp16 staging copy (kQ8 unused).
 template <bool kQ8, bool kDecode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_rope, AttnTcArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, AttnTcArgs a) {
+  // fp16 RoPE operands (prefill staging copy, q8_0 decode) or bf16 (bf16 decode).
+  constexpr bool kRopeF16 = kQ8 || !kDecode;
+  constexpr int kMmaWarp = mma_warp(kDecode);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQr = sm;
@@ -258,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup -----------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLatStages; ++i) {
-      mbar_init(&B.lat_full[i], kProducerThreads);
+      mbar_init(&B.lat_full[i], kDecode ? kProducerThreads : 1);
       mbar_init(&B.lat_empty[i], 1);
     }
     for (int i = 0; i < kRopeStages; ++i) {
@@ -316,12 +325,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::tmem_st32(tmem + lanes + kTmQ + 64 * hh + 32 * c, r);
       }
       tc::tmem_st_wait();
-      if (rank == 0) {                          // RoPE query part -> smem (bf16 as is; fp16 for q8_0)
+      if (rank == 0) {                          // RoPE query part -> smem (bf16 as is, or fp16)
         const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint4 x = rvalid ? __ldg(qp + 4 * hh + u) : make_uint4(0, 0, 0, 0);
-          st_unit(sQr, i, 4 * hh + u, kQ8 ? bf16x8_to_f16x8(x) : x);
+          st_unit(sQr, i, 4 * hh + u, kRopeF16 ? bf16x8_to_f16x8(x) : x);
         }
         tc::fence_proxy_async();
       }
@@ -516,28 +525,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < kMmaWarp) {
-    // ============================ producer =====================================
+    // ============================ loader =======================================
     const int pt = threadIdx.x - kSoftmaxWarps * 32;
-    if constexpr (kQ8) {
+    if constexpr (!kDecode) {
+      // One thread: each tile's four 64-dim latent chunks of this CTA's half
+      // (and, on rank 0, the RoPE part) by TMA, as soon as the stage is free.
+      if (pt == 0) {
+        for (int t = 0; t < n_tiles; ++t) {
+          const int ls = t % kLatStages, rs = t % kRopeStages;
+          const int key = static_cast<int>(key_base) + t * kBK;
+          if (t >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((t / kLatStages) - 1) & 1, a.wait_us, a.err))
+            break;
+          mbar_arrive_expect_tx(&B.lat_full[ls], kLatStage);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tc::tma_load_3d(sLat + ls * kLatStage + c * kChunk, &tm_cache, &B.lat_full[ls], 256 * rank + 64 * c, key, 0);
+          if (rank == 0) {
+            if (t >= kRopeStages &&
+                !mbar_wait_bounded(&B.rope_empty[rs], ((t / kRopeStages) - 1) & 1, a.wait_us, a.err))
+              break;
+            mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
+            tc::tma_load_3d(sRope + rs * kChunk, &tm_cache, &B.rope_full[rs], kLatent, key, 0);
+          }
+        }
+      }
+    } else if constexpr (kQ8) {
       if (rank == 0)
-        run_producer<true, true>(&tm_rope, a, B, sLat, sRope, 0, false, pt, key_base, kend, n_tiles);
+        run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, key_base, kend, n_tiles);
       else
-        run_producer<true, false>(&tm_rope, a, B, sLat, sRope, 1, false, pt, key_base, kend, n_tiles);
+        run_producer<true, false>(&tm_cache, a, B, sLat, sRope, 1, false, pt, key_base, kend, n_tiles);
     } else {
-      run_producer<false, false>(&tm_rope, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, key_base,
+      run_producer<false, false>(&tm_cache, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, key_base,
                                  kend, n_tiles);
     }
   } else if (lane == 0) {
     // ============================== MMA issue ==================================
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
-    constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kQ8, false, false);
+    constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kRopeF16, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
     bool ok = mbar_wait_bounded(&B.q_ready, 0, a.wait_us, a.err);
     tc::fence_after_sync();
     auto issue_qk = [&](int t) -> bool {
       const int ls = t % kLatStages, rs = t % kRopeStages, sb = t & 1;
       if (!mbar_wait_bounded(&B.lat_full[ls], (t / kLatStages) & 1, a.wait_us, a.err)) return false;
-      if (!kQ8 && rank == 0 && !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.wait_us, a.err))
+      // RoPE tiles by TMA (prefill, bf16 decode); the q8_0 producer writes them
+      // with the latent part, under lat_full.
+      if ((!kDecode || !kQ8) && rank == 0 &&
+          !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.wait_us, a.err))
         return false;
       if (t >= 2 && !mbar_wait_bounded(&B.s_free[sb], ((t >> 1) - 1) & 1, a.wait_us, a.err)) return false;
       tc::fence_after_sync();
@@ -593,7 +627,7 @@ cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_items, 
   auto kern = attn_tc_kernel<kQ8, kDecode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(2 * n_items), kThreads, kSmem, stream>>>(tm, a);
+  kern<<<dim3(2 * n_items), threads(kDecode), kSmem, stream>>>(tm, a);
   return cudaGetLastError();
 }
 
@@ -603,18 +637,19 @@ int attn_tc_rows_per_item() { return kRows; }
 
 cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
-  // Tensor map of the bf16 cache rows the kernel may address, for the RoPE
-  // tiles (64 keys x 64 dims, 128-byte swizzle); rows past n_rows read as zero.
+  // Tensor map of the cache rows the kernel may address (64 dims x 64 keys
+  // boxes, 128-byte swizzle; rows past n_rows read as zero): the fp16 staging
+  // copy for a prefill, the bf16 cache (RoPE tiles) for a bf16 decode.
   CUtensorMap tm;
-  if (!q8) {
+  if (!decode || !q8) {
     const uint64_t rows = static_cast<uint64_t>(a.n_rows);
-    cudaError_t e = make_tmap_3d(&tm, a.kv, true, kRow, rows, 1, kRow * 2, rows * kRow * 2, 64, kBK, 1);
+    cudaError_t e = make_tmap_3d(&tm, a.kv, decode, kRow, rows, 1, kRow * 2, rows * kRow * 2, 64, kBK, 1);
     if (e != cudaSuccess) return e;
   } else {
     memset(&tm, 0, sizeof(tm));
   }
-  if (q8) return decode ? launch_one<true, true>(tm, a, n_items, stream) : launch_one<true, false>(tm, a, n_items, stream);
-  return decode ? launch_one<false, true>(tm, a, n_items, stream) : launch_one<false, false>(tm, a, n_items, stream);
+  if (!decode) return launch_one<false, false>(tm, a, n_items, stream);
+  return q8 ? launch_one<true, true>(tm, a, n_items, stream) : launch_one<false, true>(tm, a, n_items, stream);
 }
 
 }  // namespace mla

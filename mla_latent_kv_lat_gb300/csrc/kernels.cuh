@@ -30,7 +30,7 @@ struct HeadGemmArgs {
 struct AttnTcArgs {
   const void* q_lat;        // fp16 [rows][H][512]
   const void* q_pe;         // bf16 [rows][H][64]
-  const void* kv;           // bf16 [n_rows][576]
+  const void* kv;           // decode: bf16 [n_rows][576]; prefill: the fp16 [n_rows][576] staging copy
   const int8_t* kv_q;       // int8 [n_rows][576]
   const uint16_t* kv_d;     // fp16 [18][ld_d]
   int64_t ld_d;
@@ -61,6 +61,10 @@ cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_item
 int attn_tc_rows_per_item();
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);
+// Cache rows [0, rows) as fp16 [rows][576] in `out` (bf16 cache when kv is
+// not null, else the q8_0 arrays kv_q / kv_d with scale row stride ld_d).
+cudaError_t launch_stage_cache_f16(const void* kv, const int8_t* kv_q, const uint16_t* kv_d, int64_t ld_d,
+                                   int64_t rows, void* out, cudaStream_t stream);
 cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream);
 int device_sm_count();
 cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d,

@@ -100,5 +100,74 @@ cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Prefill operand staging: the cache rows a prefill reads, as fp16 [rows][576]
+// (latent and RoPE parts), the type the latent tensor-core products take.
+// Every query tile of a prefill reads every visible cache row, so converting
+// once here replaces one conversion per tile inside the attention kernel.
+// bf16 -> fp16 is exact over fp16's normal range (|x| in [2^-14, 65504]);
+// q8_0 codes become fp16(scale x code), the value the decode kernel forms.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void __launch_bounds__(256) cache_bf16_to_f16_kernel(const uint4* kv, uint4* out, int64_t n_units) {
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n_units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(kv + u);
+    uint4 o;
+    float2 f;
+    f = bf16x2_to_f32(v.x); o.x = pack_f16x2(f.x, f.y);
+    f = bf16x2_to_f32(v.y); o.y = pack_f16x2(f.x, f.y);
+    f = bf16x2_to_f32(v.z); o.z = pack_f16x2(f.x, f.y);
+    f = bf16x2_to_f32(v.w); o.w = pack_f16x2(f.x, f.y);
+    out[u] = o;
+  }
+}
+
+// One thread per 16 codes (half a q8_0 block): 36 per row.
+__global__ void __launch_bounds__(256) cache_q8_0_to_f16_kernel(const int8_t* kv_q, const __half* kv_d, int64_t ld_d,
+                                                                 uint4* out, int64_t rows) {
+  const int64_t n_units = rows * (kRow / 16);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n_units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = u / (kRow / 16);
+    const int c = static_cast<int>(u % (kRow / 16));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(kv_q + row * kRow) + c);
+    const float d = __half2float(__ldg(kv_d + static_cast<int64_t>(c >> 1) * ld_d + row));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a0 = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
+      const float a1 = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
+      const float a2 = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
+      const float a3 = static_cast<float>(static_cast<int8_t>(w[k] >> 24));
+      h[2 * k] = pack_f16x2(a0 * d, a1 * d);
+      h[2 * k + 1] = pack_f16x2(a2 * d, a3 * d);
+    }
+    out[2 * u] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * u + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+unsigned stage_blocks(int64_t n_units) {
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  return static_cast<unsigned>(max(static_cast<int64_t>(1), min(cap, (n_units + 255) / 256)));
+}
+}  // namespace
+
+cudaError_t launch_stage_cache_f16(const void* kv, const int8_t* kv_q, const uint16_t* kv_d, int64_t ld_d,
+                                   int64_t rows, void* out, cudaStream_t stream) {
+  if (kv != nullptr) {
+    const int64_t n_units = rows * (kRow / 8);
+    cache_bf16_to_f16_kernel<<<stage_blocks(n_units), 256, 0, stream>>>(static_cast<const uint4*>(kv),
+                                                                         static_cast<uint4*>(out), n_units);
+  } else {
+    const int64_t n_units = rows * (kRow / 16);
+    cache_q8_0_to_f16_kernel<<<stage_blocks(n_units), 256, 0, stream>>>(
+        kv_q, reinterpret_cast<const __half*>(kv_d), ld_d, static_cast<uint4*>(out), rows);
+  }
+  return cudaGetLastError();
+}
+
 
 }  // namespace mla

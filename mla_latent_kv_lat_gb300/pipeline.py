@@ -22,14 +22,20 @@ class PrefillBuffers:
     o_lat: torch.Tensor      # fp16 [T, H, 512]
     o: torch.Tensor          # fp32 [T, H, 128]
     lse: Optional[torch.Tensor] = None
+    workspace: Optional[torch.Tensor] = None   # uint8, >= mla_prefill_workspace_size(H, n_kv)
 
 
-def prefill_buffers(T: int, H: int, device="cuda", with_lse=False) -> PrefillBuffers:
+def prefill_buffers(T: int, H: int, device="cuda", with_lse=False, n_kv: Optional[int] = None) -> PrefillBuffers:
+    """Device buffers of one prefill; with ``n_kv`` also the attention
+    workspace for a cache of that many rows (else each call allocates it)."""
+    ws = None
+    if n_kv is not None:
+        ws = torch.empty(B.mla_prefill_workspace_size(H, n_kv), dtype=torch.uint8, device=device)
     return PrefillBuffers(
         torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
         torch.empty(T, H, B.KV_LORA_RANK, dtype=torch.float16, device=device),
         torch.empty(T, H, B.V_HEAD, dtype=torch.float32, device=device),
-        torch.empty(T, H, dtype=torch.float32, device=device) if with_lse else None)
+        torch.empty(T, H, dtype=torch.float32, device=device) if with_lse else None, ws)
 
 
 def mla_prefill(q_nope, q_pe, wk_b, wv_b, q_pos0: int, *, kv=None, kv_q=None, kv_d=None,
@@ -39,13 +45,14 @@ def mla_prefill(q_nope, q_pe, wk_b, wv_b, q_pos0: int, *, kv=None, kv_q=None, kv
     Pass ``kv`` (bf16 [n_kv, 576]) or ``kv_q``/``kv_d`` (q8_0 cache)."""
     T, H = q_nope.shape[0], q_nope.shape[1]
     if bufs is None:
-        bufs = prefill_buffers(T, H, q_nope.device)
+        bufs = prefill_buffers(T, H, q_nope.device, n_kv=(kv if kv is not None else kv_q).shape[0])
     B.mla_absorb_q(q_nope, wk_b, bufs.q_lat, scale=scale, stream=stream)
     if kv is not None:
-        B.mla_attn_prefill(bufs.q_lat, q_pe, kv, q_pos0, bufs.o_lat, bufs.lse, scale=scale, stream=stream)
+        B.mla_attn_prefill(bufs.q_lat, q_pe, kv, q_pos0, bufs.o_lat, bufs.lse, scale=scale, stream=stream,
+                           workspace=bufs.workspace)
     else:
         B.mla_attn_prefill_q8_0(bufs.q_lat, q_pe, kv_q, kv_d, q_pos0, bufs.o_lat, bufs.lse, scale=scale,
-                                stream=stream)
+                                stream=stream, workspace=bufs.workspace)
     B.mla_late_decompress(bufs.o_lat, wv_b, bufs.o, scale=scale, stream=stream)
     return bufs
 

@@ -61,13 +61,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_absorb_q(_dims(), ODD, GOOD, GOOD, 4, None) == -3
     assert lib.mla_absorb_q(_dims(), GOOD, GOOD, GOOD, 0, None) == -1
     assert lib.mla_late_decompress(_dims(), GOOD, GOOD, ODD, 4, None) == -3
-    # prefill: positions must stay inside the cache
-    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 8, 3, GOOD, None, None) == -1
-    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 0, 0, GOOD, None, None) == -1
-    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, -1, GOOD, None, None) == -1
-    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, GOOD, ODD, None) == -3
-    assert lib.mla_attn_prefill(_dims(scale=0.0), GOOD, GOOD, GOOD, 10, 4, 0, GOOD, None, None) == -1
-    assert lib.mla_attn_prefill_q8_0(_dims(), GOOD, GOOD, GOOD, None, 10, 4, 0, GOOD, None, None) == -1
+    # prefill: positions must stay inside the cache; the workspace holds every row as fp16
+    pw = lib.mla_prefill_workspace_size(_dims(), 10)
+    assert pw == (10 * 1152 + 255) // 256 * 256
+    assert lib.mla_prefill_workspace_size(_dims(), 0) == 0
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 8, 3, GOOD, pw, GOOD, None, None) == -1
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 0, 0, GOOD, pw, GOOD, None, None) == -1
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, -1, GOOD, pw, GOOD, None, None) == -1
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, GOOD, pw, GOOD, ODD, None) == -3
+    assert lib.mla_attn_prefill(_dims(scale=0.0), GOOD, GOOD, GOOD, 10, 4, 0, GOOD, pw, GOOD, None, None) == -1
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, GOOD, pw - 1, GOOD, None, None) == -4
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, None, pw, GOOD, None, None) == -4
+    assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, ODD, pw, GOOD, None, None) == -3
+    assert lib.mla_attn_prefill_q8_0(_dims(), GOOD, GOOD, GOOD, None, 10, 4, 0, GOOD, pw, GOOD, None, None) == -1
     # decode: workspace size is checked on the host
     need = lib.mla_decode_workspace_size(_dims(128), 32, 32768)
     assert need > 0

@@ -279,6 +279,10 @@ def test_invalid_arguments_return_status():
     with pytest.raises(mla.MLAError) as e:
         mla.mla_attn_prefill(f16_dev(np.zeros((8, 16, 512), np.float32)), d.q_pe, d.kv, 1, o_lat)
     assert e.value.status == -1                      # q_pos0 + T > n_kv
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_attn_prefill(f16_dev(np.zeros((8, 16, 512), np.float32)), d.q_pe, d.kv, 0, o_lat,
+                             workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == -4                      # prefill workspace too small
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(mla.MLAError) as e:
         mla.mla_attn_decode(o_lat[:1], d.q_pe[:1], d.kv, torch.zeros(1, dtype=torch.int64, device="cuda"),
