@@ -57,16 +57,30 @@ constexpr int kOffRope = kOffLat + kLatStages * kLatStage;
 constexpr int kOffP = kOffRope + kRopeStages * kChunk;
 constexpr int kOffX = kOffP + kPBytes;
 constexpr int kOffAux = kOffX + 2 * kXBytes;
-// row maxima [tile parity][half][row], row sums [half][row], failure flags [tile parity][warp]
-constexpr int kAuxBytes = (4 * kRows + 2 * kRows) * 4 + 16 * 4;
+// Softmax threads per query row: each takes 64 / kTpr keys of every tile.
+// Prefill runs four (sixteen softmax warps, more latency hidden per SM
+// sub-partition); decode two, leaving registers to its producer warps.
+__host__ __device__ constexpr int tpr(bool decode) { return decode ? 2 : 2; }
+constexpr int kMaxTpr = 4, kMaxSoftmaxWarps = 4 * kMaxTpr;
+// row maxima [tile parity][thread of row][row], row sums [thread of row][row],
+// failure flags [tile parity][warp]
+constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
 constexpr int kOffBar = kOffAux + kAuxBytes;
 constexpr int kSmem = 1024 + kOffBar + 256;
-constexpr int kSoftmaxWarps = 8, kProducerWarps = 7;
+constexpr int kProducerWarps = 7;
 constexpr int kProducerThreads = kProducerWarps * 32;
+__host__ __device__ constexpr int softmax_warps(bool decode) { return 4 * tpr(decode); }
 // Loader warps: one TMA warp (prefill) or the producers (decode).
 __host__ __device__ constexpr int loader_warps(bool decode) { return decode ? kProducerWarps : 1; }
-__host__ __device__ constexpr int mma_warp(bool decode) { return kSoftmaxWarps + loader_warps(decode); }
-__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + 1) * 32; }   // decode 512, prefill 320
+__host__ __device__ constexpr int mma_warp(bool decode) { return softmax_warps(decode) + loader_warps(decode); }
+__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + 1) * 32; }   // decode 512, prefill 576
+// Registers per thread: warps go to the four SM sub-partitions in turn, and
+// each sub-partition's 16384 registers are shared by its warps (allocated in
+// steps of 8 a thread).  Decode (16 warps): 128.
+__host__ __device__ constexpr int max_regs(bool decode) {
+  return (16384 / (((mma_warp(decode) + 1 + 3) / 4) * 32)) / 8 * 8 > 255
+             ? 248 : (16384 / (((mma_warp(decode) + 1 + 3) / 4) * 32)) / 8 * 8;
+}
 // TMEM columns: Q latent half (A operand, 256 fp16 = 128 cols), two fp32 score
 // buffers of 64 columns, the fp32 output half (256 cols).
 constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 256;
@@ -217,21 +231,28 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
 // ---------------------------------------------------------------------------
 // kDecode = false: prefill from the fp16 staging copy (kQ8 unused).
 template <bool kQ8, bool kDecode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, AttnTcArgs a) {
   // fp16 RoPE operands (prefill staging copy, q8_0 decode) or bf16 (bf16 decode).
   constexpr bool kRopeF16 = kQ8 || !kDecode;
   constexpr int kMmaWarp = mma_warp(kDecode);
+  constexpr int kSoftmaxWarps = softmax_warps(kDecode);
+  constexpr int kTpr = tpr(kDecode);
+  constexpr int kKpt = kBK / kTpr;          // keys of each tile per softmax thread: 32 or 16
+  constexpr int kUpt = kKpt / 8;            // the same as 16-byte units of fp16: 4 or 2
+  constexpr int kOpt = 256 / kTpr;          // output columns (of this CTA's half) per thread: 128 or 64
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so that
+  // accesses through it stay shared-memory (not generic) accesses.
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQr = sm;
   uint8_t* sLat = sm + kOffLat;
   uint8_t* sRope = sm + kOffRope;
   uint8_t* sP = sm + kOffP;
   uint8_t* sX = sm + kOffX;
-  float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][2][128] row maxima of both halves
-  float* aux_l = aux_m + 4 * kRows;                             // [2][128] row sums
-  int* aux_fail = reinterpret_cast<int*>(aux_l + 2 * kRows);    // [2][8] per-warp failure flags
+  float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][kTpr][128] row maxima
+  float* aux_l = aux_m + 2 * kMaxTpr * kRows;                   // [kTpr][128] row sums
+  int* aux_fail = reinterpret_cast<int*>(aux_l + kMaxTpr * kRows);   // [2][16] per-warp failure flags
   Bars& B = *reinterpret_cast<Bars*>(sm + kOffBar);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
@@ -296,9 +317,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
 
   if (warp < kSoftmaxWarps) {
     // ======================= softmax / exchange / epilogue =====================
+    // kTpr threads share a query row (one per warp of the same lane quadrant):
+    // thread hh takes keys [kKpt*hh, kKpt*hh + kKpt) of every tile and output
+    // columns [kOpt*hh, kOpt*hh + kOpt) of this CTA's half.
     const int q4 = warp & 3;                    // TMEM lane quadrant
-    const int hh = warp >> 2;                   // key half of each tile: keys [32hh, 32hh+32)
-    const int partner = warp ^ 4;               // the warp holding the other 32 keys of these rows
+    const int hh = warp >> 2;                   // which share of the row
     const int i = q4 * 32 + lane;               // query row == TMEM lane
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
     const bool rvalid = i < nvalid;
@@ -310,27 +333,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
       lim = rvalid ? a.q_pos0 + static_cast<int>(qrow / H) : kend - 1;
     }
     const float c2 = a.scale_log2;              // raw score -> log2 units
-    // Q latent half -> TMEM (fp16 A operand), this thread: dims [128hh, 128hh+128) of the half.
+    // Q latent half -> TMEM (fp16 A operand), this thread: dims [kOpt*hh, kOpt*hh + kOpt) of the half.
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
-                                                        256 * rank + 128 * hh);
+                                                        256 * rank + kOpt * hh);
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kOpt / 64; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = rvalid ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
           r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
         }
-        tc::tmem_st32(tmem + lanes + kTmQ + 64 * hh + 32 * c, r);
+        tc::tmem_st32(tmem + lanes + kTmQ + (kOpt / 2) * hh + 32 * c, r);
       }
       tc::tmem_st_wait();
       if (rank == 0) {                          // RoPE query part -> smem (bf16 as is, or fp16)
         const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 x = rvalid ? __ldg(qp + 4 * hh + u) : make_uint4(0, 0, 0, 0);
-          st_unit(sQr, i, 4 * hh + u, kRopeF16 ? bf16x8_to_f16x8(x) : x);
+        for (int u = 0; u < 8 / kTpr; ++u) {
+          const uint4 x = rvalid ? __ldg(qp + (8 / kTpr) * hh + u) : make_uint4(0, 0, 0, 0);
+          st_unit(sQr, i, (8 / kTpr) * hh + u, kRopeF16 ? bf16x8_to_f16x8(x) : x);
         }
         tc::fence_proxy_async();
       }
@@ -341,60 +364,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
     const uint32_t peer_x = tc::mapa(smem_u32(sX), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(&B.x_full[0]), peer);
     const uint32_t peer_xempty = tc::mapa(smem_u32(&B.x_empty[0]), peer);
-    const int bar_id = 1 + q4;                  // named barrier of the two warps sharing these rows
+    const int bar_id = 1 + q4;                  // named barrier of the kTpr warps sharing these rows
     float m_run = -INFINITY, l_h = 0.f;
     // A wait that gave up makes the warp "dead": it skips every later wait,
-    // tensor-memory access and arrival, but still meets its partner warp at
-    // every named barrier, so neither warp of a pair can be left waiting.
+    // tensor-memory access and arrival, but still meets its partner warps at
+    // every named barrier, so no warp of a row group can be left waiting.
     bool dead = false;
     auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
       if (!dead) dead = !wait_all(bar, parity, a);
     };
 
-    // Read this thread's 32 partial scores of tile t, free the score buffer,
-    // keep them as fp16 pairs and send the same pairs to the peer.
-    auto fetch_send = [&](int t, uint32_t (&own)[16]) {
+    // Read this thread's kKpt partial scores of tile t, free the score buffer
+    // and keep them as fp16 pairs.
+    auto fetch = [&](int t, uint32_t (&own)[kKpt / 2]) {
       const int sb = t & 1;
       wait_ok(&B.s_full[sb], (t >> 1) & 1);
       if (dead) return;
       tc::fence_after_sync();
-      uint32_t r[32];
-      tc::tmem_ld32(tmem + lanes + kTmS + sb * 64 + 32 * hh, r);
+      uint32_t r[kKpt];
+      tc::tmem_ld<kKpt>(tmem + lanes + kTmS + sb * 64 + kKpt * hh, r);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       mbar_arrive(&B.s_free[sb]);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+      for (int k = 0; k < kKpt / 2; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+    };
+
+    // Send tile t's fp16 partials to the peer, once it has finished with the
+    // exchange buffer's previous contents (tile t-2).
+    auto send = [&](int t, const uint32_t (&own)[kKpt / 2]) {
+      const int sb = t & 1;
       if (t >= 2 && !dead)
         dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1, a.wait_us,
                                                                       a.err));
       if (dead) return;
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        tc::st_async_v4(peer_x + sb * kXBytes + ((4 * hh + g) * kRows + i) * 16,
+      for (int g = 0; g < kUpt; ++g)
+        tc::st_async_v4(peer_x + sb * kXBytes + ((kUpt * hh + g) * kRows + i) * 16,
                         make_uint4(own[4 * g], own[4 * g + 1], own[4 * g + 2], own[4 * g + 3]), peer_xfull + sb * 8);
       if (threadIdx.x == 0) mbar_arrive_expect_tx(&B.x_full[sb], kXBytes);
     };
 
-    // Meet the partner warp (same rows, other key half): publish `val` and this
-    // warp's state, return the partner's value.
-    auto pair_exchange = [&](float* slot_mine, const float* slot_theirs, float val, int phase) -> float {
-      *slot_mine = val;
-      if (lane == 0) aux_fail[(phase & 1) * 8 + warp] = dead ? 1 : 0;
-      tc::named_bar_sync(bar_id, 64);
-      if (aux_fail[(phase & 1) * 8 + partner] != 0) dead = true;
-      return *slot_theirs;
+    // Meet the other warps of this row group: publish `val` (in slot
+    // base[hh][row]) and this warp's state; the caller then reads the group's
+    // values from base.
+    auto group_meet = [&](float* base, float val, int phase) {
+      base[hh * kRows + i] = val;
+      if (lane == 0) aux_fail[(phase & 1) * kMaxSoftmaxWarps + warp] = dead ? 1 : 0;
+      tc::named_bar_sync(bar_id, kTpr * 32);
+#pragma unroll
+      for (int g = 0; g < kTpr; ++g)
+        if (aux_fail[(phase & 1) * kMaxSoftmaxWarps + q4 + 4 * g] != 0) dead = true;
     };
 
     // Softmax of tile j from the two fp16 partials.
-    auto process = [&](int j, const uint32_t (&own)[16]) {
+    // Softmax of tile j from the two fp16 partials; tile j+1's partials go to
+    // the peer in the middle, late enough that the peer has long released the
+    // buffer and early enough that they arrive before it needs them.
+    auto process = [&](int j, const uint32_t (&own)[kKpt / 2], const uint32_t (&nxt)[kKpt / 2]) {
       const int xb = j & 1;
       if (!dead)
         dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.wait_us, a.err));
-      float s[32];
+      float s[kKpt];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint4 pv = *reinterpret_cast<const uint4*>(sX + xb * kXBytes + ((4 * hh + g) * kRows + i) * 16);
+      for (int g = 0; g < kUpt; ++g) {
+        const uint4 pv = *reinterpret_cast<const uint4*>(sX + xb * kXBytes + ((kUpt * hh + g) * kRows + i) * 16);
         const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -403,24 +437,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
           s[8 * g + 2 * e + 1] = tc::add_f16hi_f32(pw[e], x.y);
         }
       }
-      const int k0 = j * kBK + 32 * hh;
-      if (k0 + 31 > lim) {
+      const int k0 = j * kBK + kKpt * hh;
+      if (k0 + kKpt - 1 > lim) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
+        for (int k = 0; k < kKpt; ++k)
           if (k0 + k > lim) s[k] = -INFINITY;
       }
-      // Row maximum of this half as a tree (short dependency chain).
-      float mx[16];
+      // Row maximum of this share as a tree (short dependency chain).
+      float mx[kKpt / 2];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+      for (int k = 0; k < kKpt / 2; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = kKpt / 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
-      const float mt = mx[0] * c2;
-      const float mo = pair_exchange(&aux_m[((j & 1) * 2 + hh) * kRows + i],
-                                     &aux_m[((j & 1) * 2 + (1 - hh)) * kRows + i], mt, j);
-      const float mrow = fmaxf(mt, mo);
+      float* mslot = aux_m + (j & 1) * kMaxTpr * kRows;
+      group_meet(mslot, mx[0] * c2, j);
+      float mrow = mslot[i];
+#pragma unroll
+      for (int g = 1; g < kTpr; ++g) mrow = fmaxf(mrow, mslot[g * kRows + i]);
+      if (j + 1 < n_tiles) send(j + 1, nxt);
       // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
       float alpha = 1.f;
       if (mrow > m_run + kRescaleThreshold) {
@@ -429,10 +465,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
         l_h *= alpha;
       }
       // p = 2^(s*c - m) on packed halves; the row sum stays in fp32.
-      uint32_t pk[16];
+      uint32_t pk[kKpt / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};        // four independent partial sums
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < kKpt / 2; ++k) {
         pk[k] = tc::exp2_approx_f16x2(pack_f16x2(fmaf(s[2 * k], c2, -m_run), fmaf(s[2 * k + 1], c2, -m_run)));
         ls[k & 3] = tc::add_f16hi_f32(pk[k], tc::add_f16lo_f32(pk[k], ls[k & 3]));
       }
@@ -444,9 +480,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
           tc::fence_after_sync();
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kOpt / 32; ++c) {
               uint32_t o[32];
-              const uint32_t col = tmem + lanes + kTmO + 128 * hh + 32 * c;
+              const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
               tc::tmem_ld32(col, o);
               tc::tmem_ld_wait();
 #pragma unroll
@@ -459,8 +495,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
       }
       if (dead) return;
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        st_unit(sP, i, 4 * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+      for (int g = 0; g < kUpt; ++g)
+        st_unit(sP, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
       tc::fence_proxy_async();
       tc::fence_before_sync();
       mbar_arrive(&B.p_full);
@@ -472,28 +508,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
     };
 
     // One loop body (a register copy per tile keeps the hot code small).
-    uint32_t own[16], nxt[16];
-    fetch_send(0, own);
+    uint32_t own[kKpt / 2], nxt[kKpt / 2];
+    fetch(0, own);
+    send(0, own);
 #pragma unroll 1
     for (int j = 0; j < n_tiles; ++j) {
-      if (j + 1 < n_tiles) fetch_send(j + 1, nxt);
-      process(j, own);
+      if (j + 1 < n_tiles) fetch(j + 1, nxt);
+      process(j, own, nxt);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) own[k] = nxt[k];
+      for (int k = 0; k < kKpt / 2; ++k) own[k] = nxt[k];
     }
     wait_ok(&B.pv_done, (n_tiles - 1) & 1);
-    const float l_other = pair_exchange(&aux_l[hh * kRows + i], &aux_l[(1 - hh) * kRows + i], l_h, n_tiles);
+    group_meet(aux_l, l_h, n_tiles);
     if (!dead) {
       tc::fence_after_sync();
-      const float l_row = hh == 0 ? l_h + l_other : l_other + l_h;
+      float l_row = aux_l[i];                   // the same order in every thread of the row
+#pragma unroll
+      for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
       const float inv = 1.f / l_row;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kOpt / 32; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(tmem + lanes + kTmO + 128 * hh + 32 * c, o);
+        tc::tmem_ld32(tmem + lanes + kTmO + kOpt * hh + 32 * c, o);
         tc::tmem_ld_wait();
         if (!rvalid) continue;
-        const int col = 256 * static_cast<int>(rank) + 128 * hh + 32 * c;
+        const int col = 256 * static_cast<int>(rank) + kOpt * hh + 32 * c;
         if constexpr (kDecode) {
           uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (slot0 + i) * kLatent + col);
 #pragma unroll
@@ -558,51 +597,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(kDecode), 1)
       run_producer<false, false>(&tm_cache, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, key_base,
                                  kend, n_tiles);
     }
-  } else if (lane == 0) {
+  } else {
     // ============================== MMA issue ==================================
+    // The whole warp runs this loop (see mma_ss_warp); one lane issues.
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
     constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kRopeF16, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
-    bool ok = mbar_wait_bounded(&B.q_ready, 0, a.wait_us, a.err);
+    bool ok = wait_all(&B.q_ready, 0, a);
     tc::fence_after_sync();
     auto issue_qk = [&](int t) -> bool {
       const int ls = t % kLatStages, rs = t % kRopeStages, sb = t & 1;
-      if (!mbar_wait_bounded(&B.lat_full[ls], (t / kLatStages) & 1, a.wait_us, a.err)) return false;
+      if (!wait_all(&B.lat_full[ls], (t / kLatStages) & 1, a)) return false;
       // RoPE tiles by TMA (prefill, bf16 decode); the q8_0 producer writes them
       // with the latent part, under lat_full.
       if ((!kDecode || !kQ8) && rank == 0 &&
-          !mbar_wait_bounded(&B.rope_full[rs], (t / kRopeStages) & 1, a.wait_us, a.err))
+          !wait_all(&B.rope_full[rs], (t / kRopeStages) & 1, a))
         return false;
-      if (t >= 2 && !mbar_wait_bounded(&B.s_free[sb], ((t >> 1) - 1) & 1, a.wait_us, a.err)) return false;
+      if (t >= 2 && !wait_all(&B.s_free[sb], ((t >> 1) - 1) & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t k0 = smem_u32(sLat + ls * kLatStage);
       const uint32_t d = tmem + kTmS + sb * 64;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks)        // latent half: A = Q from TMEM
-        tc::mma_ts(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024),
+        tc::mma_ts_warp(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024),
                    idesc_lat, ks > 0 ? 1u : 0u);
       if (rank == 0) {
         const uint32_t q0 = smem_u32(sQr), r0 = smem_u32(sRope + rs * kChunk);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)       // RoPE part: A = Q_pe from smem
-          tc::mma_ss(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024), idesc_rope,
+          tc::mma_ss_warp(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024), idesc_rope,
                      1u);
-        tc::mma_commit(&B.rope_empty[rs]);
+        tc::mma_commit_warp(&B.rope_empty[rs]);
       }
-      tc::mma_commit(&B.s_full[sb]);
+      tc::mma_commit_warp(&B.s_full[sb]);
       return true;
     };
     auto issue_pv = [&](int t) -> bool {
-      if (!mbar_wait_bounded(&B.p_full, t & 1, a.wait_us, a.err)) return false;
+      if (!wait_all(&B.p_full, t & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t v0 = smem_u32(sLat + (t % kLatStages) * kLatStage);
       const uint32_t p0 = smem_u32(sP);
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks)
-        tc::mma_ss(tmem + kTmO, tc::sdesc_sw128(p0 + ks * 32, 16, 1024),
+        tc::mma_ss_warp(tmem + kTmO, tc::sdesc_sw128(p0 + ks * 32, 16, 1024),
                    tc::sdesc_sw128(v0 + ks * 2048, kChunk, 1024), idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-      tc::mma_commit(&B.lat_empty[t % kLatStages]);
-      tc::mma_commit(&B.pv_done);
+      tc::mma_commit_warp(&B.lat_empty[t % kLatStages]);
+      tc::mma_commit_warp(&B.pv_done);
       return true;
     };
     // Scores run three tiles ahead of P.V.

@@ -107,18 +107,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(w_full, 0, g.wait_us, g.err);
+    {   // whole warp, converged; one lane issues (see mma_ss_warp)
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(w_full, 0, g.wait_us, g.err));
       tc::fence_after_sync();
       constexpr uint32_t idesc = tc::idesc_f16(128, NSUB, kAbsorb, false, true);
       for (int i = 0; ok && i < n_tiles; ++i) {
         for (int j = 0; ok && j < C::NS; ++j) {
           const int job = i * C::NS + j, slot = job % C::SLOTS;
-          if (job >= C::SLOTS) ok = mbar_wait_bounded(&acc_empty[slot], ((job / C::SLOTS) - 1) & 1, g.wait_us, g.err);
+          if (job >= C::SLOTS)
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[slot], ((job / C::SLOTS) - 1) & 1, g.wait_us, g.err));
           tc::fence_after_sync();
           for (int kc = 0; ok && kc < C::KC; ++kc) {
             const int u = i * C::KC + kc, st = u % kStages;
-            if (j == 0) ok = mbar_wait_bounded(&a_full[st], (u / kStages) & 1, g.wait_us, g.err);
+            if (j == 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a_full[st], (u / kStages) & 1, g.wait_us, g.err));
             if (!ok) break;
             tc::fence_after_sync();
             const uint32_t a0 = smem_u32(sA + st * kChunkBytes);
@@ -128,11 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int k = kc * 64 + ks * 16;
               const uint64_t ad = tc::sdesc_sw128(a0 + ks * 32, 16, 1024);
               const uint64_t bd = tc::sdesc_sw128(b0 + (k / 16) * 2048, C::W_CHUNK, 1024);
-              tc::mma_ss(tmem + slot * NSUB, ad, bd, idesc, (kc | ks) != 0);
+              tc::mma_ss_warp(tmem + slot * NSUB, ad, bd, idesc, (kc | ks) != 0);
             }
-            if (j == C::NS - 1) tc::mma_commit(&a_empty[st]);
+            if (j == C::NS - 1) tc::mma_commit_warp(&a_empty[st]);
           }
-          tc::mma_commit(&acc_full[slot]);
+          tc::mma_commit_warp(&acc_full[slot]);
         }
       }
       if (!ok) abort_flag = 1;
