@@ -73,13 +73,17 @@ __host__ __device__ constexpr int softmax_warps(bool decode) { return 4 * tpr(de
 // Loader warps: one TMA warp (prefill) or the producers (decode).
 __host__ __device__ constexpr int loader_warps(bool decode) { return decode ? kProducerWarps : 1; }
 __host__ __device__ constexpr int mma_warp(bool decode) { return softmax_warps(decode) + loader_warps(decode); }
-__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + 1) * 32; }   // decode 512, prefill 576
+// Prefill issues the score MMAs and the P.V MMAs from two warps, so that a
+// score tile waiting for its cache tile never holds back a P.V; decode has no
+// warp to spare and issues both from one.
+__host__ __device__ constexpr int mma_warps(bool decode) { return decode ? 1 : 2; }
+__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + mma_warps(decode)) * 32; }
 // Registers per thread: warps go to the four SM sub-partitions in turn, and
 // each sub-partition's 16384 registers are shared by its warps (allocated in
 // steps of 8 a thread).  Decode (16 warps): 128.
 __host__ __device__ constexpr int max_regs(bool decode) {
-  return (16384 / (((mma_warp(decode) + 1 + 3) / 4) * 32)) / 8 * 8 > 255
-             ? 248 : (16384 / (((mma_warp(decode) + 1 + 3) / 4) * 32)) / 8 * 8;
+  return (16384 / (((threads(decode) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
+             ? 248 : (16384 / (((threads(decode) / 32 + 3) / 4) * 32)) / 8 * 8;
 }
 // TMEM columns: Q latent half (A operand, 256 fp16 = 128 cols), two fp32 score
 // buffers of 64 columns, the fp32 output half (256 cols).
@@ -376,9 +380,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
 
     // Read this thread's kKpt partial scores of tile t, free the score buffer
     // and keep them as fp16 pairs.
-    auto fetch = [&](int t, uint32_t (&own)[kKpt / 2]) {
+    // `ready`: an earlier non-blocking check already saw the phase complete.
+    auto fetch = [&](int t, uint32_t (&own)[kKpt / 2], bool ready) {
       const int sb = t & 1;
-      wait_ok(&B.s_full[sb], (t >> 1) & 1);
+      if (!ready) wait_ok(&B.s_full[sb], (t >> 1) & 1);
       if (dead) return;
       tc::fence_after_sync();
       uint32_t r[kKpt];
@@ -410,6 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     // values from base.
     auto group_meet = [&](float* base, float val, int phase) {
       base[hh * kRows + i] = val;
+      if constexpr (kTpr == 1) return;           // the row has one thread: nothing to meet
       if (lane == 0) aux_fail[(phase & 1) * kMaxSoftmaxWarps + warp] = dead ? 1 : 0;
       tc::named_bar_sync(bar_id, kTpr * 32);
 #pragma unroll
@@ -418,12 +424,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     };
 
     // Softmax of tile j from the two fp16 partials.
-    // Softmax of tile j from the two fp16 partials; tile j+1's partials go to
-    // the peer in the middle, late enough that the peer has long released the
-    // buffer and early enough that they arrive before it needs them.
-    auto process = [&](int j, const uint32_t (&own)[kKpt / 2], const uint32_t (&nxt)[kKpt / 2]) {
+    // Softmax of tile j from the two fp16 partials.
+    auto process = [&](int j, const uint32_t (&own)[kKpt / 2], bool ready) {
       const int xb = j & 1;
-      if (!dead)
+      if (!dead && !ready)
         dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.wait_us, a.err));
       float s[kKpt];
 #pragma unroll
@@ -456,7 +460,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       float mrow = mslot[i];
 #pragma unroll
       for (int g = 1; g < kTpr; ++g) mrow = fmaxf(mrow, mslot[g * kRows + i]);
-      if (j + 1 < n_tiles) send(j + 1, nxt);
       // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
       float alpha = 1.f;
       if (mrow > m_run + kRescaleThreshold) {
@@ -509,12 +512,21 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
 
     // One loop body (a register copy per tile keeps the hot code small).
     uint32_t own[kKpt / 2], nxt[kKpt / 2];
-    fetch(0, own);
+    fetch(0, own, false);
     send(0, own);
 #pragma unroll 1
     for (int j = 0; j < n_tiles; ++j) {
-      if (j + 1 < n_tiles) fetch(j + 1, nxt);
-      process(j, own, nxt);
+      // Check both phases this iteration needs first, so that their latencies
+      // overlap; a phase not yet complete is waited for where it is needed.
+      const bool s_test = mbar_test(&B.s_full[(j + 1) & 1], ((j + 1) >> 1) & 1);
+      const bool x_test = tc::mbar_test_cluster(&B.x_full[j & 1], (j >> 1) & 1);
+      const bool s_ready = __all_sync(0xffffffffu, s_test) && j + 1 < n_tiles;
+      const bool x_ready = __all_sync(0xffffffffu, x_test);
+      if (j + 1 < n_tiles) {
+        fetch(j + 1, nxt, s_ready);
+        send(j + 1, nxt);
+      }
+      process(j, own, x_ready);
 #pragma unroll
       for (int k = 0; k < kKpt / 2; ++k) own[k] = nxt[k];
     }
@@ -599,7 +611,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     }
   } else {
     // ============================== MMA issue ==================================
-    // The whole warp runs this loop (see mma_ss_warp); one lane issues.
+    // The whole warp runs this loop (see mma_ss_warp); one lane issues.  With
+    // two MMA warps, the first issues the score MMAs, the second P.V; the P.V
+    // commit frees the cache stage, which the score MMA of the same tile had
+    // finished reading before the softmax could produce P.
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
     constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kRopeF16, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
@@ -645,11 +660,22 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       tc::mma_commit_warp(&B.pv_done);
       return true;
     };
-    // Scores run three tiles ahead of P.V.
-    for (int t = 0; ok && t < 3 && t < n_tiles; ++t) ok = issue_qk(t);
-    for (int t = 0; ok && t < n_tiles; ++t) {
-      ok = issue_pv(t);
-      if (ok && t + 3 < n_tiles) ok = issue_qk(t + 3);
+    if constexpr (mma_warps(kDecode) == 2) {
+      // Each stream in order, each as soon as its operands are ready (the
+      // score MMAs are bounded by the two score buffers, so they run at most
+      // three tiles ahead of P.V).
+      if (warp == kMmaWarp) {
+        for (int t = 0; ok && t < n_tiles; ++t) ok = issue_qk(t);
+      } else {
+        for (int t = 0; ok && t < n_tiles; ++t) ok = issue_pv(t);
+      }
+    } else {
+      // Scores run three tiles ahead of P.V.
+      for (int t = 0; ok && t < 3 && t < n_tiles; ++t) ok = issue_qk(t);
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        ok = issue_pv(t);
+        if (ok && t + 3 < n_tiles) ok = issue_qk(t + 3);
+      }
     }
   }
 

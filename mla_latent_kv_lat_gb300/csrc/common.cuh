@@ -109,6 +109,21 @@ MLA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking check of phase `parity` (acquire at CTA scope when it returns
+// true).  The result arrives like a load's, so a check issued early overlaps
+// its latency with other work until the branch that consumes it.
+MLA_DEVINL bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait that lets the hardware suspend the thread for up to `ns`
 // nanoseconds (or until the phase completes) instead of returning at once.
 // A waiting warp then takes no issue slots from the warps doing the work.

@@ -58,11 +58,18 @@ MLA_DEVINL void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-// N consecutive columns (N = 16 or 32).
+// N consecutive columns (N = 16, 32 or 64).
 template <int N>
 MLA_DEVINL void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
-  static_assert(N == 16 || N == 32, "tmem_ld width");
-  if constexpr (N == 16) tmem_ld16(taddr, r); else tmem_ld32(taddr, r);
+  static_assert(N == 16 || N == 32 || N == 64, "tmem_ld width");
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, r);
+  } else if constexpr (N == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  }
 }
 MLA_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -220,6 +227,18 @@ MLA_DEVINL bool mbar_try_wait_cluster_suspend(uint64_t* bar, uint32_t parity, ui
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_test with cluster-scope acquire.
+MLA_DEVINL bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
