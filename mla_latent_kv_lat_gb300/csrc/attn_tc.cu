@@ -61,10 +61,11 @@ constexpr int kOffAux = kOffX + 2 * kXBytes;
 // Prefill runs four (sixteen softmax warps, more latency hidden per SM
 // sub-partition); decode two, leaving registers to its producer warps.
 __host__ __device__ constexpr int tpr(bool decode) { return decode ? 2 : 2; }
-constexpr int kMaxTpr = 4, kMaxSoftmaxWarps = 4 * kMaxTpr;
+constexpr int kMaxTpr = 2, kMaxSoftmaxWarps = 4 * kMaxTpr;
 // row maxima [tile parity][thread of row][row], row sums [thread of row][row],
 // failure flags [tile parity][warp]
-constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
+// plus, for the epilogue warps, the row sums [item parity][row]
+constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows + 2 * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
 constexpr int kOffBar = kOffAux + kAuxBytes;
 constexpr int kSmem = 1024 + kOffBar + 256;
 constexpr int kProducerWarps = 7;
@@ -72,7 +73,14 @@ constexpr int kProducerThreads = kProducerWarps * 32;
 __host__ __device__ constexpr int softmax_warps(bool decode) { return 4 * tpr(decode); }
 // Loader warps: one TMA warp (prefill) or the producers (decode).
 __host__ __device__ constexpr int loader_warps(bool decode) { return decode ? kProducerWarps : 1; }
-__host__ __device__ constexpr int mma_warp(bool decode) { return softmax_warps(decode) + loader_warps(decode); }
+// Prefill has four more warps (one per TMEM lane quadrant) that load each
+// item's Q into tensor memory as soon as the previous item's last score MMA
+// has completed, and write each item's output once its last P.V has: the
+// softmax warps go straight from one item's last tile to the next item's
+// first.  Decode has no registers to spare for them; its softmax warps do both.
+__host__ __device__ constexpr int epi_warps(bool decode) { return decode ? 0 : 4; }
+__host__ __device__ constexpr int loader_warp(bool decode) { return softmax_warps(decode) + epi_warps(decode); }
+__host__ __device__ constexpr int mma_warp(bool decode) { return loader_warp(decode) + loader_warps(decode); }
 // Prefill issues the score MMAs and the P.V MMAs from two warps, so that a
 // score tile waiting for its cache tile never holds back a P.V; decode has no
 // warp to spare and issues both from one.
@@ -102,7 +110,11 @@ struct Bars {
   uint64_t x_empty[2];
   uint64_t p_full;
   uint64_t pv_done;
-  uint64_t q_ready;
+  uint64_t q_ready;   // arrival per item: Q of the next item is in TMEM
+  uint64_t o_free;    // arrival per item: the epilogue has read O
+  uint64_t q_free;    // commit per item (prefill): its last score MMA has completed
+  uint64_t o_ready;   // commit per item (prefill): its last P.V has completed
+  uint64_t l_ready[2];   // arrival per item (prefill), by item parity: row sums in aux
   uint32_t tmem;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -193,40 +205,122 @@ struct Producer {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Work items.  With G clusters, cluster c runs one item per round r: item
+// index rG + c in even rounds and rG + (G-1-c) in odd ones.  Prefill items
+// come longest first, so the snake order pairs long with short and keeps the
+// clusters' totals close.  Every role of both CTAs walks the same sequence,
+// and every ring and barrier phase counts tiles across items, so one item's
+// first tiles load and start while the previous item drains.
+// ---------------------------------------------------------------------------
+MLA_DEVINL int round_item(int c, int g, int r) { return r * g + ((r & 1) ? g - 1 - c : c); }
+
+struct Item {
+  int64_t key_base;   // cache row of item key 0
+  int kend;           // keys [0, kend) of this item (0: nothing to do)
+  int nvalid;         // valid query rows
+  int64_t qrow0;      // flattened (token, head) index (prefill) or sequence x H (decode) of row 0
+  int64_t slot0;      // decode: partial slot of row 0
+  int n_tiles;
+};
+
+template <bool kDecode>
+MLA_DEVINL Item item_at(const AttnTcArgs& a, int idx) {
+  Item it;
+  if constexpr (kDecode) {
+    const int b = idx / a.n_split, s = idx % a.n_split;
+    const int len = a.seq_len[b];
+    const int lo = s * a.chunk;
+    it.key_base = a.seq_start[b] + lo;
+    it.kend = lo < len ? min(len - lo, a.chunk) : 0;
+    it.nvalid = a.n_head;
+    it.qrow0 = static_cast<int64_t>(b) * a.n_head;
+    it.slot0 = static_cast<int64_t>(idx) * a.n_head;
+  } else {
+    const int item = a.n_items - 1 - idx;     // long prefill rows (late tokens) first
+    const int64_t rho0 = static_cast<int64_t>(item) * kRows;
+    it.nvalid = static_cast<int>(min(static_cast<int64_t>(kRows), a.n_qrows - rho0));
+    it.kend = a.q_pos0 + static_cast<int>((rho0 + it.nvalid - 1) / a.n_head) + 1;
+    it.key_base = 0;
+    it.qrow0 = rho0;
+    it.slot0 = 0;
+  }
+  it.n_tiles = (it.kend + kBK - 1) / kBK;
+  return it;
+}
+
+// Walks this cluster's tiles in order across its items.
+template <bool kDecode>
+struct TileCursor {
+  const AttnTcArgs* a;
+  int c, g, r;        // cluster, cluster count, round
+  Item it;
+  int t;              // tile within the item
+  MLA_DEVINL bool done() const { return r * g >= a->n_items; }
+  MLA_DEVINL void load_round() {
+    const int idx = round_item(c, g, r);
+    if (idx < a->n_items) it = item_at<kDecode>(*a, idx); else it.n_tiles = 0;
+  }
+  MLA_DEVINL void skip_empty() {
+    while (!done() && t >= it.n_tiles) {
+      ++r;
+      t = 0;
+      if (!done()) load_round();
+    }
+  }
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
+    a = &args; c = cluster; g = clusters; r = 0; t = 0;
+    if (!done()) load_round();
+    skip_empty();
+  }
+  MLA_DEVINL bool valid() const { return !done(); }
+  MLA_DEVINL void next() { ++t; skip_empty(); }
+};
+
 // kRope: this producer writes the RoPE ring (q8_0 cache, rank 0).  With a bf16
 // cache the RoPE tiles come by TMA, issued when `tma_rope` is set (rank 0).
+// Tile u counts this cluster's tiles across items.
 template <bool kQ8, bool kRope>
 MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Bars& B, uint8_t* sLat,
-                             uint8_t* sRope, int rank, bool tma_rope, int pt, int64_t key_base, int kend,
-                             int n_tiles) {
+                             uint8_t* sRope, int rank, bool tma_rope, int pt, int first, int stride) {
   using P = Producer<kQ8, kRope>;
   const bool uses_rope = kRope || tma_rope;
+  TileCursor<true> cur;
+  cur.init(a, first, stride);
+  if (!cur.valid()) return;
   P x, y;
-  // Tile j+1's loads are in flight while tile j is converted and stored.
-  auto step = [&](int j, P& cur, P& nxt) -> bool {
-    if (j + 1 < n_tiles) nxt.load(a, rank, pt, key_base, (j + 1) * kBK, kend);
-    const int ls = j % kLatStages, rs = j % kRopeStages;
-    if (j >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((j / kLatStages) - 1) & 1, a.wait_us, a.err))
+  int64_t cur_row = cur.it.key_base + static_cast<int64_t>(cur.t) * kBK;
+  x.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
+  cur.next();
+  // Tile u+1's loads are in flight while tile u is converted and stored.
+  auto step = [&](int u, P& now, P& nxt) -> bool {
+    const bool more = cur.valid();
+    const int64_t nxt_row = more ? cur.it.key_base + static_cast<int64_t>(cur.t) * kBK : 0;
+    if (more) {
+      nxt.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
+      cur.next();
+    }
+    const int ls = u % kLatStages, rs = u % kRopeStages;
+    if (u >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((u / kLatStages) - 1) & 1, a.wait_us, a.err))
       return false;
-    if (uses_rope && j >= kRopeStages &&
-        !mbar_wait_bounded(&B.rope_empty[rs], ((j / kRopeStages) - 1) & 1, a.wait_us, a.err))
+    if (uses_rope && u >= kRopeStages &&
+        !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
       return false;
     if constexpr (!kQ8) {                     // bf16 RoPE keys by TMA, straight into the B-operand layout
       if (tma_rope && pt == 0) {
         mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
-        tc::tma_load_3d(sRope + rs * kChunk, tm_rope, &B.rope_full[rs], kLatent,
-                        static_cast<int>(key_base + j * kBK), 0);
+        tc::tma_load_3d(sRope + rs * kChunk, tm_rope, &B.rope_full[rs], kLatent, static_cast<int>(cur_row), 0);
       }
     }
-    cur.store(sLat + ls * kLatStage, sRope + rs * kChunk, pt);
+    now.store(sLat + ls * kLatStage, sRope + rs * kChunk, pt);
     tc::fence_proxy_async();
     mbar_arrive(&B.lat_full[ls]);
-    return true;
+    cur_row = nxt_row;
+    return more;
   };
-  if (n_tiles > 0) x.load(a, rank, pt, key_base, 0, kend);
-  for (int j = 0; j < n_tiles; j += 2) {
-    if (!step(j, x, y)) return;
-    if (j + 1 < n_tiles && !step(j + 1, y, x)) return;
+  for (int u = 0;; u += 2) {
+    if (!step(u, x, y)) return;
+    if (!step(u + 1, y, x)) return;
   }
 }
 
@@ -240,6 +334,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
   // fp16 RoPE operands (prefill staging copy, q8_0 decode) or bf16 (bf16 decode).
   constexpr bool kRopeF16 = kQ8 || !kDecode;
   constexpr int kMmaWarp = mma_warp(kDecode);
+  constexpr bool kEpi = epi_warps(kDecode) > 0;
+  constexpr int kLoaderWarp = loader_warp(kDecode);
   constexpr int kSoftmaxWarps = softmax_warps(kDecode);
   constexpr int kTpr = tpr(kDecode);
   constexpr int kKpt = kBK / kTpr;          // keys of each tile per softmax thread: 32 or 16
@@ -256,38 +352,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
   uint8_t* sX = sm + kOffX;
   float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][kTpr][128] row maxima
   float* aux_l = aux_m + 2 * kMaxTpr * kRows;                   // [kTpr][128] row sums
-  int* aux_fail = reinterpret_cast<int*>(aux_l + kMaxTpr * kRows);   // [2][16] per-warp failure flags
+  float* aux_lrow = aux_l + kMaxTpr * kRows;                    // [2][128] row sums for the epilogue warps
+  int* aux_fail = reinterpret_cast<int*>(aux_lrow + 2 * kRows); // [2][8] per-warp failure flags
   Bars& B = *reinterpret_cast<Bars*>(sm + kOffBar);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.n_head;
-
-  // ---- work item -----------------------------------------------------------
-  const int n_items = gridDim.x >> 1;
-  const int item = n_items - 1 - static_cast<int>(blockIdx.x >> 1);   // long prefill rows first
-  int64_t key_base = 0;     // cache row of item key 0
-  int kend = 0;             // keys [0, kend) of this item
-  int nvalid = 0;           // valid query rows
-  int64_t qrow0 = 0;        // flattened (token, head) index of row 0
-  int64_t slot0 = 0;        // decode: partial slot of row 0
-  if constexpr (kDecode) {
-    const int b = item / a.n_split, s = item % a.n_split;
-    const int len = a.seq_len[b];
-    const int lo = s * a.chunk;
-    if (lo >= len) return;                    // both CTAs of the pair leave together
-    key_base = a.seq_start[b] + lo;
-    kend = min(len - lo, a.chunk);
-    nvalid = H;
-    qrow0 = static_cast<int64_t>(b) * H;
-    slot0 = static_cast<int64_t>(item) * H;
-  } else {
-    const int64_t rho0 = static_cast<int64_t>(item) * kRows;
-    nvalid = static_cast<int>(min(static_cast<int64_t>(kRows), a.n_qrows - rho0));
-    kend = a.q_pos0 + static_cast<int>((rho0 + nvalid - 1) / H) + 1;
-    qrow0 = rho0;
-  }
-  const int n_tiles = (kend + kBK - 1) / kBK;
+  const int first = static_cast<int>(blockIdx.x >> 1);      // this cluster's first item index
+  const int stride = static_cast<int>(gridDim.x >> 1);      // clusters
 
   // ---- setup -----------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -307,7 +380,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     }
     mbar_init(&B.p_full, kSoftmaxWarps * 32);
     mbar_init(&B.pv_done, 1);
-    mbar_init(&B.q_ready, kSoftmaxWarps * 32);
+    mbar_init(&B.q_ready, kEpi ? 128 : kSoftmaxWarps * 32);
+    mbar_init(&B.o_free, kEpi ? 128 : kSoftmaxWarps * 32);
+    mbar_init(&B.q_free, 1);
+    mbar_init(&B.o_ready, 1);
+    mbar_init(&B.l_ready[0], kSoftmaxWarps * 32);
+    mbar_init(&B.l_ready[1], kSoftmaxWarps * 32);
     tc::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -328,48 +406,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     const int hh = warp >> 2;                   // which share of the row
     const int i = q4 * 32 + lane;               // query row == TMEM lane
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
-    const bool rvalid = i < nvalid;
-    const int64_t qrow = qrow0 + i;
-    int lim;                                    // last visible key index (item-relative)
-    if constexpr (kDecode) {
-      lim = kend - 1;
-    } else {
-      lim = rvalid ? a.q_pos0 + static_cast<int>(qrow / H) : kend - 1;
-    }
     const float c2 = a.scale_log2;              // raw score -> log2 units
-    // Q latent half -> TMEM (fp16 A operand), this thread: dims [kOpt*hh, kOpt*hh + kOpt) of the half.
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
-                                                        256 * rank + kOpt * hh);
-#pragma unroll 1
-      for (int c = 0; c < kOpt / 64; ++c) {
-        uint32_t r[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = rvalid ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-        }
-        tc::tmem_st32(tmem + lanes + kTmQ + (kOpt / 2) * hh + 32 * c, r);
-      }
-      tc::tmem_st_wait();
-      if (rank == 0) {                          // RoPE query part -> smem (bf16 as is, or fp16)
-        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
-#pragma unroll
-        for (int u = 0; u < 8 / kTpr; ++u) {
-          const uint4 x = rvalid ? __ldg(qp + (8 / kTpr) * hh + u) : make_uint4(0, 0, 0, 0);
-          st_unit(sQr, i, (8 / kTpr) * hh + u, kRopeF16 ? bf16x8_to_f16x8(x) : x);
-        }
-        tc::fence_proxy_async();
-      }
-      tc::fence_before_sync();
-      mbar_arrive(&B.q_ready);
-    }
-
     const uint32_t peer_x = tc::mapa(smem_u32(sX), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(&B.x_full[0]), peer);
     const uint32_t peer_xempty = tc::mapa(smem_u32(&B.x_empty[0]), peer);
     const int bar_id = 1 + q4;                  // named barrier of the kTpr warps sharing these rows
-    float m_run = -INFINITY, l_h = 0.f;
     // A wait that gave up makes the warp "dead": it skips every later wait,
     // tensor-memory access and arrival, but still meets its partner warps at
     // every named barrier, so no warp of a row group can be left waiting.
@@ -378,12 +419,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       if (!dead) dead = !wait_all(bar, parity, a);
     };
 
-    // Read this thread's kKpt partial scores of tile t, free the score buffer
-    // and keep them as fp16 pairs.
-    // `ready`: an earlier non-blocking check already saw the phase complete.
-    auto fetch = [&](int t, uint32_t (&own)[kKpt / 2], bool ready) {
-      const int sb = t & 1;
-      if (!ready) wait_ok(&B.s_full[sb], (t >> 1) & 1);
+    // Read this thread's kKpt partial scores of tile u (counted across
+    // items), free the score buffer and keep them as fp16 pairs.  `ready`: an
+    // earlier non-blocking check already saw the phase complete.
+    auto fetch = [&](int u, uint32_t (&own)[kKpt / 2], bool ready) {
+      const int sb = u & 1;
+      if (!ready) wait_ok(&B.s_full[sb], (u >> 1) & 1);
       if (dead) return;
       tc::fence_after_sync();
       uint32_t r[kKpt];
@@ -395,12 +436,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       for (int k = 0; k < kKpt / 2; ++k) own[k] = pack_f16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
     };
 
-    // Send tile t's fp16 partials to the peer, once it has finished with the
-    // exchange buffer's previous contents (tile t-2).
-    auto send = [&](int t, const uint32_t (&own)[kKpt / 2]) {
-      const int sb = t & 1;
-      if (t >= 2 && !dead)
-        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((t >> 1) - 1) & 1, a.wait_us,
+    // Send tile u's fp16 partials to the peer, once it has finished with the
+    // exchange buffer's previous contents (tile u-2).
+    auto send = [&](int u, const uint32_t (&own)[kKpt / 2]) {
+      const int sb = u & 1;
+      if (u >= 2 && !dead)
+        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_empty[sb], ((u >> 1) - 1) & 1, a.wait_us,
                                                                       a.err));
       if (dead) return;
 #pragma unroll
@@ -423,177 +464,331 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
         if (aux_fail[(phase & 1) * kMaxSoftmaxWarps + q4 + 4 * g] != 0) dead = true;
     };
 
-    // Softmax of tile j from the two fp16 partials.
-    // Softmax of tile j from the two fp16 partials.
-    auto process = [&](int j, const uint32_t (&own)[kKpt / 2], bool ready) {
-      const int xb = j & 1;
-      if (!dead && !ready)
-        dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (j >> 1) & 1, a.wait_us, a.err));
-      float s[kKpt];
+    uint32_t own[kKpt / 2], nxt[kKpt / 2];
+    int u0 = 0;                                 // this item's first tile, counted across items
+    int k = 0;                                  // items done
+#pragma unroll 1
+    for (int rnd = 0; rnd * stride < a.n_items; ++rnd) {
+      const int idx = round_item(first, stride, rnd);
+      if (idx >= a.n_items) continue;
+      const Item it = item_at<kDecode>(a, idx);
+      if (it.n_tiles == 0) continue;
+      const bool rvalid = i < it.nvalid;
+      const int64_t qrow = it.qrow0 + i;
+      int lim;                                  // last visible key index (item-relative)
+      if constexpr (kDecode) {
+        lim = it.kend - 1;
+      } else {
+        lim = rvalid ? a.q_pos0 + static_cast<int>(qrow / H) : it.kend - 1;
+      }
+      // Decode: Q latent half -> TMEM (fp16 A operand), this thread: dims
+      // [kOpt*hh, kOpt*hh + kOpt) of the half.  The previous item's score MMAs
+      // have all completed (this thread read every one of their results), so
+      // the Q region and the RoPE query tile are free.  (Prefill: the epilogue
+      // warps do this.)
+      if constexpr (!kEpi) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
+                                                          256 * rank + kOpt * hh);
+        // All loads first (one round trip), then the stores.
+        uint32_t r[kOpt / 64][32];
+        uint4 qpe[8 / kTpr];
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
 #pragma unroll
-      for (int g = 0; g < kUpt; ++g) {
-        const uint4 pv = *reinterpret_cast<const uint4*>(sX + xb * kXBytes + ((kUpt * hh + g) * kRows + i) * 16);
-        const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+        for (int c = 0; c < kOpt / 64; ++c)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = f16x2_to_f32(own[4 * g + e]);
-          s[8 * g + 2 * e] = tc::add_f16lo_f32(pw[e], x.x);
-          s[8 * g + 2 * e + 1] = tc::add_f16hi_f32(pw[e], x.y);
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = rvalid ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
+            r[c][4 * v] = x.x; r[c][4 * v + 1] = x.y; r[c][4 * v + 2] = x.z; r[c][4 * v + 3] = x.w;
+          }
+#pragma unroll
+        for (int v = 0; v < 8 / kTpr; ++v)
+          qpe[v] = rank == 0 && rvalid ? __ldg(qp + (8 / kTpr) * hh + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < kOpt / 64; ++c) tc::tmem_st32(tmem + lanes + kTmQ + (kOpt / 2) * hh + 32 * c, r[c]);
+        tc::tmem_st_wait();
+        if (rank == 0) {                        // RoPE query part -> smem (bf16 as is, or fp16)
+#pragma unroll
+          for (int v = 0; v < 8 / kTpr; ++v) st_unit(sQr, i, (8 / kTpr) * hh + v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+          tc::fence_proxy_async();
         }
+        tc::fence_before_sync();
+        mbar_arrive(&B.q_ready);
       }
-      const int k0 = j * kBK + kKpt * hh;
-      if (k0 + kKpt - 1 > lim) {
+
+      float m_run = -INFINITY, l_h = 0.f;
+      const int n = it.n_tiles;
+
+      // Softmax of item tile t (tile u = u0 + t overall) from the two fp16 partials.
+      auto process = [&](int t, const uint32_t (&own_t)[kKpt / 2], bool ready) {
+        const int u = u0 + t, xb = u & 1;
+        if (!dead && !ready)
+          dead = !__all_sync(0xffffffffu, tc::mbar_wait_cluster_bounded(&B.x_full[xb], (u >> 1) & 1, a.wait_us, a.err));
+        float s[kKpt];
 #pragma unroll
-        for (int k = 0; k < kKpt; ++k)
-          if (k0 + k > lim) s[k] = -INFINITY;
+        for (int g = 0; g < kUpt; ++g) {
+          const uint4 pv = *reinterpret_cast<const uint4*>(sX + xb * kXBytes + ((kUpt * hh + g) * kRows + i) * 16);
+          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = f16x2_to_f32(own_t[4 * g + e]);
+            s[8 * g + 2 * e] = tc::add_f16lo_f32(pw[e], x.x);
+            s[8 * g + 2 * e + 1] = tc::add_f16hi_f32(pw[e], x.y);
+          }
+        }
+        const int k0 = t * kBK + kKpt * hh;
+        if (k0 + kKpt - 1 > lim) {
+#pragma unroll
+          for (int e = 0; e < kKpt; ++e)
+            if (k0 + e > lim) s[e] = -INFINITY;
+        }
+        // Row maximum of this share as a tree (short dependency chain).
+        float mx[kKpt / 2];
+#pragma unroll
+        for (int e = 0; e < kKpt / 2; ++e) mx[e] = fmaxf(s[2 * e], s[2 * e + 1]);
+#pragma unroll
+        for (int w = kKpt / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+        float* mslot = aux_m + (u & 1) * kMaxTpr * kRows;
+        group_meet(mslot, mx[0] * c2, u);
+        float mrow = mslot[i];
+#pragma unroll
+        for (int g = 1; g < kTpr; ++g) mrow = fmaxf(mrow, mslot[g * kRows + i]);
+        // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
+        float alpha = 1.f;
+        if (mrow > m_run + kRescaleThreshold) {
+          alpha = tc::exp2_approx(m_run - mrow);
+          m_run = mrow;
+          l_h *= alpha;
+        }
+        // p = 2^(s*c - m) on packed halves; the row sum stays in fp32.
+        uint32_t pk[kKpt / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};      // four independent partial sums
+#pragma unroll
+        for (int e = 0; e < kKpt / 2; ++e) {
+          pk[e] = tc::exp2_approx_f16x2(pack_f16x2(fmaf(s[2 * e], c2, -m_run), fmaf(s[2 * e + 1], c2, -m_run)));
+          ls[e & 3] = tc::add_f16hi_f32(pk[e], tc::add_f16lo_f32(pk[e], ls[e & 3]));
+        }
+        l_h += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P.V of tile u-1 has finished: the P buffer is free and O is stable.
+        // (A new item's O restarts with its first P.V: nothing to rescale.)
+        if (u >= 1) {
+          wait_ok(&B.pv_done, (u - 1) & 1);
+          if (!dead && t >= 1) {
+            tc::fence_after_sync();
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+              for (int c = 0; c < kOpt / 32; ++c) {
+                uint32_t o[32];
+                const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
+                tc::tmem_ld32(col, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tc::tmem_st32(col, o);
+              }
+              tc::tmem_st_wait();
+            }
+          }
+        }
+        if (dead) return;
+#pragma unroll
+        for (int g = 0; g < kUpt; ++g)
+          st_unit(sP, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        mbar_arrive(&B.p_full);
+        // This warp has long finished reading exchange buffer xb (every value read
+        // from it fed the scores above): tell the peer it may refill it.  A relaxed
+        // arrival suffices and avoids the ~1.4k-cycle cluster-scope release.
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_xempty + xb * 8);
+      };
+
+      // One loop body (a register copy per tile keeps the hot code small).
+      fetch(u0, own, false);
+      send(u0, own);
+#pragma unroll 1
+      for (int t = 0; t < n; ++t) {
+        const int u = u0 + t;
+        // Check both phases this tile needs first, so that their latencies
+        // overlap; a phase not yet complete is waited for where it is needed.
+        const bool s_test = mbar_test(&B.s_full[(u + 1) & 1], ((u + 1) >> 1) & 1);
+        const bool x_test = tc::mbar_test_cluster(&B.x_full[u & 1], (u >> 1) & 1);
+        const bool s_ready = __all_sync(0xffffffffu, s_test) && t + 1 < n;
+        const bool x_ready = __all_sync(0xffffffffu, x_test);
+        if (t + 1 < n) {
+          fetch(u + 1, nxt, s_ready);
+          send(u + 1, nxt);
+        }
+        process(t, own, x_ready);
+#pragma unroll
+        for (int e = 0; e < kKpt / 2; ++e) own[e] = nxt[e];
       }
-      // Row maximum of this share as a tree (short dependency chain).
-      float mx[kKpt / 2];
+      // ---- end of item -----------------------------------------------------------
+      if constexpr (kEpi) {
+        // Prefill: hand the row sums to the epilogue warps and go on.
+        group_meet(aux_l, l_h, u0 + n);
+        float l_row = aux_l[i];                 // the same order in every thread of the row
 #pragma unroll
-      for (int k = 0; k < kKpt / 2; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
-#pragma unroll
-      for (int w = kKpt / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
-      float* mslot = aux_m + (j & 1) * kMaxTpr * kRows;
-      group_meet(mslot, mx[0] * c2, j);
-      float mrow = mslot[i];
-#pragma unroll
-      for (int g = 1; g < kTpr; ++g) mrow = fmaxf(mrow, mslot[g * kRows + i]);
-      // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
-      float alpha = 1.f;
-      if (mrow > m_run + kRescaleThreshold) {
-        alpha = tc::exp2_approx(m_run - mrow);
-        m_run = mrow;
-        l_h *= alpha;
-      }
-      // p = 2^(s*c - m) on packed halves; the row sum stays in fp32.
-      uint32_t pk[kKpt / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};        // four independent partial sums
-#pragma unroll
-      for (int k = 0; k < kKpt / 2; ++k) {
-        pk[k] = tc::exp2_approx_f16x2(pack_f16x2(fmaf(s[2 * k], c2, -m_run), fmaf(s[2 * k + 1], c2, -m_run)));
-        ls[k & 3] = tc::add_f16hi_f32(pk[k], tc::add_f16lo_f32(pk[k], ls[k & 3]));
-      }
-      l_h += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P.V of tile j-1 has finished: the P buffer is free and O is stable.
-      if (j >= 1) {
-        wait_ok(&B.pv_done, (j - 1) & 1);
+        for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
+        if (hh == 0) aux_lrow[(k & 1) * kRows + i] = l_row;
+        if (rank == 0 && hh == 0 && rvalid && a.lse != nullptr) a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
+        mbar_arrive(&B.l_ready[k & 1]);
+      } else {
+        // Decode: O / l -> the fp32 partials, with the running max and sum.
+        wait_ok(&B.pv_done, (u0 + n - 1) & 1);
+        group_meet(aux_l, l_h, u0 + n);
         if (!dead) {
           tc::fence_after_sync();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-            for (int c = 0; c < kOpt / 32; ++c) {
-              uint32_t o[32];
-              const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
-              tc::tmem_ld32(col, o);
-              tc::tmem_ld_wait();
+          float l_row = aux_l[i];               // the same order in every thread of the row
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tc::tmem_st32(col, o);
-            }
-            tc::tmem_st_wait();
+          for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
+          const float inv = 1.f / l_row;
+#pragma unroll 1
+          for (int c = 0; c < kOpt / 32; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(tmem + lanes + kTmO + kOpt * hh + 32 * c, o);
+            tc::tmem_ld_wait();
+            if (!rvalid) continue;
+            const int col = 256 * static_cast<int>(rank) + kOpt * hh + 32 * c;
+            uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (it.slot0 + i) * kLatent + col);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * inv),
+                                  __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
+                                  __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
+                                  __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
           }
+          if (rank == 0 && hh == 0 && rvalid) {
+            a.ws_ml[2 * (it.slot0 + i)] = m_run;
+            a.ws_ml[2 * (it.slot0 + i) + 1] = l_row;
+          }
+          // O has been read: the next item's first P.V may overwrite it.
+          tc::fence_before_sync();
+          mbar_arrive(&B.o_free);
         }
       }
-      if (dead) return;
-#pragma unroll
-      for (int g = 0; g < kUpt; ++g)
-        st_unit(sP, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      mbar_arrive(&B.p_full);
-      // This warp has long finished reading exchange buffer xb (every value read
-      // from it fed the scores above): tell the peer it may refill it.  A relaxed
-      // arrival suffices and avoids the ~1.4k-cycle cluster-scope release.
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_xempty + xb * 8);
-    };
-
-    // One loop body (a register copy per tile keeps the hot code small).
-    uint32_t own[kKpt / 2], nxt[kKpt / 2];
-    fetch(0, own, false);
-    send(0, own);
-#pragma unroll 1
-    for (int j = 0; j < n_tiles; ++j) {
-      // Check both phases this iteration needs first, so that their latencies
-      // overlap; a phase not yet complete is waited for where it is needed.
-      const bool s_test = mbar_test(&B.s_full[(j + 1) & 1], ((j + 1) >> 1) & 1);
-      const bool x_test = tc::mbar_test_cluster(&B.x_full[j & 1], (j >> 1) & 1);
-      const bool s_ready = __all_sync(0xffffffffu, s_test) && j + 1 < n_tiles;
-      const bool x_ready = __all_sync(0xffffffffu, x_test);
-      if (j + 1 < n_tiles) {
-        fetch(j + 1, nxt, s_ready);
-        send(j + 1, nxt);
-      }
-      process(j, own, x_ready);
-#pragma unroll
-      for (int k = 0; k < kKpt / 2; ++k) own[k] = nxt[k];
+      u0 += n;
+      ++k;
     }
-    wait_ok(&B.pv_done, (n_tiles - 1) & 1);
-    group_meet(aux_l, l_h, n_tiles);
-    if (!dead) {
+  } else if (kEpi && warp < kLoaderWarp) {
+    // ======================= Q loading and epilogue (prefill) ==================
+    // Warp 8+q serves TMEM lane quadrant q: thread = query row i, the whole
+    // 256-column half of the row.  Per item k: once item k-1's last score MMA
+    // has completed (q_free), Q of item k -> TMEM (and Q_pe -> smem on rank 0),
+    // then q_ready; then, once item k-1's last P.V has completed (o_ready) and
+    // its row sums are in (l_ready), O / l -> o_lat and o_free.
+    const int q4 = warp & 3;
+    const int i = q4 * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    bool ok = true;
+    auto epilogue = [&](const Item& pv, int kk) {
+      ok = ok && wait_all(&B.o_ready, kk & 1, a);
+      ok = ok && wait_all(&B.l_ready[kk & 1], (kk >> 1) & 1, a);
+      if (!ok) return;
       tc::fence_after_sync();
-      float l_row = aux_l[i];                   // the same order in every thread of the row
-#pragma unroll
-      for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
-      const float inv = 1.f / l_row;
+      const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
+      const bool valid = i < pv.nvalid;
+      uint16_t* dst = static_cast<uint16_t*>(a.o_lat) + (pv.qrow0 + i) * kLatent + 256 * rank;
 #pragma unroll 1
-      for (int c = 0; c < kOpt / 32; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(tmem + lanes + kTmO + kOpt * hh + 32 * c, o);
+        tc::tmem_ld32(tmem + lanes + kTmO + 32 * c, o);
         tc::tmem_ld_wait();
-        if (!rvalid) continue;
-        const int col = 256 * static_cast<int>(rank) + kOpt * hh + 32 * c;
-        if constexpr (kDecode) {
-          uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (slot0 + i) * kLatent + col);
+        if (!valid) continue;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * inv),
-                                __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
-                                __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
-                                __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o_lat) + qrow * kLatent + col);
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_f16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+          w.y = pack_f16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+          w.z = pack_f16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+          w.w = pack_f16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = w;
+        }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&B.o_free);
+    };
+    Item prev;
+    int k = 0;
+#pragma unroll 1
+    for (int rnd = 0; ok && rnd * stride < a.n_items; ++rnd) {
+      const int idx = round_item(first, stride, rnd);
+      if (idx >= a.n_items) continue;
+      const Item it = item_at<kDecode>(a, idx);
+      if (it.n_tiles == 0) continue;
+      if (k > 0) ok = wait_all(&B.q_free, (k - 1) & 1, a);
+      if (!ok) break;
+      tc::fence_after_sync();
+      const bool rvalid = i < it.nvalid;
+      const int64_t qrow = it.qrow0 + i;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
+                                                        256 * rank);
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {          // two rounds of 16 loads (128 dims each)
+        uint32_t r[2][32];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_f16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_f16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_f16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_f16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = rvalid ? __ldg(src + (2 * h2 + c) * 8 + v) : make_uint4(0, 0, 0, 0);
+            r[c][4 * v] = x.x; r[c][4 * v + 1] = x.y; r[c][4 * v + 2] = x.z; r[c][4 * v + 3] = x.w;
           }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tc::tmem_st32(tmem + lanes + kTmQ + 32 * (2 * h2 + c), r[c]);
+      }
+      tc::tmem_st_wait();
+      if (rank == 0) {                          // RoPE query part -> smem, fp16
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
+        uint4 qpe[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) st_unit(sQr, i, v, bf16x8_to_f16x8(qpe[v]));
+        tc::fence_proxy_async();
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&B.q_ready);
+      // Bring the next item's queries into L2 meanwhile.
+      if (lane == 0 && q4 == 0 && (rnd + 1) * stride < a.n_items) {
+        const int nidx = round_item(first, stride, rnd + 1);
+        if (nidx < a.n_items) {
+          const Item nx = item_at<kDecode>(a, nidx);
+          if (rank == 0)
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_lat) + nx.qrow0 * kLatent,
+                            static_cast<uint32_t>(nx.nvalid) * kLatent * 2);
+          else
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_pe) + nx.qrow0 * kRope,
+                            static_cast<uint32_t>(nx.nvalid) * kRope * 2);
         }
       }
-      if (rank == 0 && hh == 0 && rvalid) {
-        if constexpr (kDecode) {
-          a.ws_ml[2 * (slot0 + i)] = m_run;
-          a.ws_ml[2 * (slot0 + i) + 1] = l_row;
-        } else if (a.lse != nullptr) {
-          a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
-        }
-      }
+      if (k > 0) epilogue(prev, k - 1);
+      prev = it;
+      ++k;
     }
+    if (ok && k > 0) epilogue(prev, k - 1);
   } else if (warp < kMmaWarp) {
     // ============================ loader =======================================
-    const int pt = threadIdx.x - kSoftmaxWarps * 32;
+    const int pt = threadIdx.x - kLoaderWarp * 32;
     if constexpr (!kDecode) {
       // One thread: each tile's four 64-dim latent chunks of this CTA's half
       // (and, on rank 0, the RoPE part) by TMA, as soon as the stage is free.
       if (pt == 0) {
-        for (int t = 0; t < n_tiles; ++t) {
-          const int ls = t % kLatStages, rs = t % kRopeStages;
-          const int key = static_cast<int>(key_base) + t * kBK;
-          if (t >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((t / kLatStages) - 1) & 1, a.wait_us, a.err))
+        TileCursor<false> cur;
+        cur.init(a, first, stride);
+        for (int u = 0; cur.valid(); ++u, cur.next()) {
+          const int ls = u % kLatStages, rs = u % kRopeStages;
+          const int key = static_cast<int>(cur.it.key_base) + cur.t * kBK;
+          if (u >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((u / kLatStages) - 1) & 1, a.wait_us, a.err))
             break;
           mbar_arrive_expect_tx(&B.lat_full[ls], kLatStage);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tc::tma_load_3d(sLat + ls * kLatStage + c * kChunk, &tm_cache, &B.lat_full[ls], 256 * rank + 64 * c, key, 0);
           if (rank == 0) {
-            if (t >= kRopeStages &&
-                !mbar_wait_bounded(&B.rope_empty[rs], ((t / kRopeStages) - 1) & 1, a.wait_us, a.err))
+            if (u >= kRopeStages &&
+                !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
               break;
             mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
             tc::tma_load_3d(sRope + rs * kChunk, &tm_cache, &B.rope_full[rs], kLatent, key, 0);
@@ -602,61 +797,64 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       }
     } else if constexpr (kQ8) {
       if (rank == 0)
-        run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, key_base, kend, n_tiles);
+        run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, first, stride);
       else
-        run_producer<true, false>(&tm_cache, a, B, sLat, sRope, 1, false, pt, key_base, kend, n_tiles);
+        run_producer<true, false>(&tm_cache, a, B, sLat, sRope, 1, false, pt, first, stride);
     } else {
-      run_producer<false, false>(&tm_cache, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, key_base,
-                                 kend, n_tiles);
+      run_producer<false, false>(&tm_cache, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, first,
+                                 stride);
     }
   } else {
     // ============================== MMA issue ==================================
     // The whole warp runs this loop (see mma_ss_warp); one lane issues.  With
     // two MMA warps, the first issues the score MMAs, the second P.V; the P.V
     // commit frees the cache stage, which the score MMA of the same tile had
-    // finished reading before the softmax could produce P.
+    // finished reading before the softmax could produce P.  Tiles u count
+    // this cluster's tiles across items.
     constexpr uint32_t idesc_lat = tc::idesc_f16(128, kBK, false, false, false);
     constexpr uint32_t idesc_rope = tc::idesc_f16(128, kBK, !kRopeF16, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(128, 256, false, false, true);
-    bool ok = wait_all(&B.q_ready, 0, a);
-    tc::fence_after_sync();
-    auto issue_qk = [&](int t) -> bool {
-      const int ls = t % kLatStages, rs = t % kRopeStages, sb = t & 1;
-      if (!wait_all(&B.lat_full[ls], (t / kLatStages) & 1, a)) return false;
+    bool ok = true;
+    auto issue_qk = [&](int u) -> bool {
+      const int ls = u % kLatStages, rs = u % kRopeStages, sb = u & 1;
+      if (!wait_all(&B.lat_full[ls], (u / kLatStages) & 1, a)) return false;
       // RoPE tiles by TMA (prefill, bf16 decode); the q8_0 producer writes them
       // with the latent part, under lat_full.
       if ((!kDecode || !kQ8) && rank == 0 &&
-          !wait_all(&B.rope_full[rs], (t / kRopeStages) & 1, a))
+          !wait_all(&B.rope_full[rs], (u / kRopeStages) & 1, a))
         return false;
-      if (t >= 2 && !wait_all(&B.s_free[sb], ((t >> 1) - 1) & 1, a)) return false;
+      if (u >= 2 && !wait_all(&B.s_free[sb], ((u >> 1) - 1) & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t k0 = smem_u32(sLat + ls * kLatStage);
       const uint32_t d = tmem + kTmS + sb * 64;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks)        // latent half: A = Q from TMEM
         tc::mma_ts_warp(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024),
-                   idesc_lat, ks > 0 ? 1u : 0u);
+                        idesc_lat, ks > 0 ? 1u : 0u);
       if (rank == 0) {
         const uint32_t q0 = smem_u32(sQr), r0 = smem_u32(sRope + rs * kChunk);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)       // RoPE part: A = Q_pe from smem
-          tc::mma_ss_warp(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024), idesc_rope,
-                     1u);
+          tc::mma_ss_warp(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024),
+                          idesc_rope, 1u);
         tc::mma_commit_warp(&B.rope_empty[rs]);
       }
       tc::mma_commit_warp(&B.s_full[sb]);
       return true;
     };
-    auto issue_pv = [&](int t) -> bool {
-      if (!wait_all(&B.p_full, t & 1, a)) return false;
+    // `t0`: first tile of its item (O restarts; the previous item's epilogue
+    // must have read O, the k-th arrival on o_free).
+    auto issue_pv = [&](int u, bool t0, int k) -> bool {
+      if (!wait_all(&B.p_full, u & 1, a)) return false;
+      if (t0 && k > 0 && !wait_all(&B.o_free, (k - 1) & 1, a)) return false;
       tc::fence_after_sync();
-      const uint32_t v0 = smem_u32(sLat + (t % kLatStages) * kLatStage);
+      const uint32_t v0 = smem_u32(sLat + (u % kLatStages) * kLatStage);
       const uint32_t p0 = smem_u32(sP);
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks)
         tc::mma_ss_warp(tmem + kTmO, tc::sdesc_sw128(p0 + ks * 32, 16, 1024),
-                   tc::sdesc_sw128(v0 + ks * 2048, kChunk, 1024), idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-      tc::mma_commit_warp(&B.lat_empty[t % kLatStages]);
+                        tc::sdesc_sw128(v0 + ks * 2048, kChunk, 1024), idesc_pv, (!t0 || ks > 0) ? 1u : 0u);
+      tc::mma_commit_warp(&B.lat_empty[u % kLatStages]);
       tc::mma_commit_warp(&B.pv_done);
       return true;
     };
@@ -664,17 +862,46 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       // Each stream in order, each as soon as its operands are ready (the
       // score MMAs are bounded by the two score buffers, so they run at most
       // three tiles ahead of P.V).
-      if (warp == kMmaWarp) {
-        for (int t = 0; ok && t < n_tiles; ++t) ok = issue_qk(t);
-      } else {
-        for (int t = 0; ok && t < n_tiles; ++t) ok = issue_pv(t);
+      int u = 0, k = 0;
+      for (int r = 0; ok && r * stride < a.n_items; ++r) {
+        const int idx = round_item(first, stride, r);
+        if (idx >= a.n_items) continue;
+        const Item it = item_at<kDecode>(a, idx);
+        if (it.n_tiles == 0) continue;
+        if (warp == kMmaWarp) {
+          // Q of item k in TMEM (the k-th arrival on q_ready).
+          ok = wait_all(&B.q_ready, k & 1, a);
+          tc::fence_after_sync();
+          for (int t = 0; ok && t < it.n_tiles; ++t) ok = issue_qk(u + t);
+          if (ok && kEpi) tc::mma_commit_warp(&B.q_free);     // Q and Q_pe may be replaced
+        } else {
+          for (int t = 0; ok && t < it.n_tiles; ++t) ok = issue_pv(u + t, t == 0, k);
+          if (ok && kEpi) tc::mma_commit_warp(&B.o_ready);    // O of item k is final
+        }
+        u += it.n_tiles;
+        ++k;
       }
     } else {
-      // Scores run three tiles ahead of P.V.
-      for (int t = 0; ok && t < 3 && t < n_tiles; ++t) ok = issue_qk(t);
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        ok = issue_pv(t);
-        if (ok && t + 3 < n_tiles) ok = issue_qk(t + 3);
+      // One warp: scores run up to three tiles ahead of P.V within an item; at
+      // an item boundary the next item's first scores wait until its Q is in
+      // TMEM, which the softmax loads only after it has produced every P of
+      // the current item, so they are issued after the current item's last P.V.
+      int u = 0, k = 0;
+      for (int r = 0; ok && r * stride < a.n_items; ++r) {
+        const int idx = round_item(first, stride, r);
+        if (idx >= a.n_items) continue;
+        const Item it = item_at<kDecode>(a, idx);
+        if (it.n_tiles == 0) continue;
+        const int n = it.n_tiles;
+        ok = wait_all(&B.q_ready, k & 1, a);
+        tc::fence_after_sync();
+        for (int t = 0; ok && t < 3 && t < n; ++t) ok = issue_qk(u + t);
+        for (int t = 0; ok && t < n; ++t) {
+          ok = issue_pv(u + t, t == 0, k);
+          if (ok && t + 3 < n) ok = issue_qk(u + t + 3);
+        }
+        u += n;
+        ++k;
       }
     }
   }
@@ -689,11 +916,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
 }
 
 template <bool kQ8, bool kDecode>
-cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_items, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_clusters, cudaStream_t stream) {
   auto kern = attn_tc_kernel<kQ8, kDecode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(2 * n_items), threads(kDecode), kSmem, stream>>>(tm, a);
+  kern<<<dim3(2 * n_clusters), threads(kDecode), kSmem, stream>>>(tm, a);
   return cudaGetLastError();
 }
 
@@ -701,8 +928,15 @@ cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_items, 
 
 int attn_tc_rows_per_item() { return kRows; }
 
-cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream) {
+cudaError_t launch_attn_tc(const AttnTcArgs& args, bool q8, bool decode, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;
+  AttnTcArgs a = args;
+  a.n_items = n_items;
+  // Prefill: persistent clusters, one per SM pair (one CTA per SM fits), each
+  // looping over its items.  Decode: one cluster per item (the item lengths
+  // are known only on the device, so the hardware's dynamic scheduling of
+  // clusters balances them).
+  const int n_clusters = decode ? n_items : min(n_items, max(1, device_sm_count() / 2));
   // Tensor map of the cache rows the kernel may address (64 dims x 64 keys
   // boxes, 128-byte swizzle; rows past n_rows read as zero): the fp16 staging
   // copy for a prefill, the bf16 cache (RoPE tiles) for a bf16 decode.
@@ -714,8 +948,8 @@ cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_item
   } else {
     memset(&tm, 0, sizeof(tm));
   }
-  if (!decode) return launch_one<false, false>(tm, a, n_items, stream);
-  return q8 ? launch_one<true, true>(tm, a, n_items, stream) : launch_one<false, true>(tm, a, n_items, stream);
+  if (!decode) return launch_one<false, false>(tm, a, n_clusters, stream);
+  return q8 ? launch_one<true, true>(tm, a, n_clusters, stream) : launch_one<false, true>(tm, a, n_clusters, stream);
 }
 
 }  // namespace mla

@@ -51,6 +51,7 @@ struct AttnTcArgs {
   float* ws_ml;             // fp32 [B * n_split][H][2]   running max (log2 units) and sum
   int* err;
   uint32_t wait_us;
+  int n_items;              // set by launch_attn_tc
 };
 
 // 3-D tiled tensor map of 16-bit elements with 128-byte swizzle (zero fill outside).

@@ -179,6 +179,13 @@ MLA_DEVINL void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// Bring `bytes` (multiple of 16) of global memory at `p` (16-byte aligned)
+// into L2 without waiting.
+MLA_DEVINL void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 MLA_DEVINL void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
