@@ -132,7 +132,9 @@ int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q
                           void* o_lat, float* lse, void* stream);
 
 /* Bytes of device workspace mla_attn_decode / mla_attn_decode_q8_0 need for
- * B sequences no longer than max_len (split-KV partial results).  Returns 0
+ * B sequences (split-KV partial results): the keys of all sequences are split
+ * evenly over G = (SM count / 2) clusters, which makes at most B + G - 1
+ * pieces of H x 2056 bytes each.  max_len only bounds the lengths.  Returns 0
  * for invalid arguments.  The value depends only on the arguments and the
  * current device.                                                             */
 size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_len);
@@ -173,8 +175,8 @@ int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_
  * cudaMalloc, cudaFree or allocating library routine).
  * Limit: mla_decode_workspace_size(dims, B, max_len) must not exceed
  *   33554432 bytes (32 MiB); larger requests return MLA_ERR_WORKSPACE with
- *   nothing launched.  E.g. B = 8 sequences up to 16384 tokens at 128 heads
- *   need 16.8 MB.
+ *   nothing launched.  On GB300 (G = 76) at 128 heads: B = 8 needs 21.8 MB,
+ *   B = 52 fits, B = 53 does not.
  * Sharing: every call uses the same array.  Calls whose work overlaps on the
  *   GPU (different streams without ordering, several host threads) race on it
  *   and corrupt each other's results; order them on one stream or with

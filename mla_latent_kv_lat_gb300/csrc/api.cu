@@ -52,22 +52,10 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; 
 
 constexpr float kLog2eF = 1.4426950408889634f;
 
-// Split-KV plan of the decode kernels: keys per split and splits per sequence.
-struct DecodePlan {
-  int chunk;
-  int n_split;
-};
-
-DecodePlan decode_plan(int32_t max_len) {
-  DecodePlan p;
-  p.chunk = 2048;
-  p.n_split = static_cast<int>((static_cast<int64_t>(max_len) + p.chunk - 1) / p.chunk);
-  return p;
-}
-
-size_t decode_ws_bytes(int H, int32_t B, int32_t max_len) {
-  const DecodePlan p = decode_plan(max_len);
-  const size_t slots = static_cast<size_t>(B) * p.n_split * H;
+// Decode workspace: one partial per piece (a cluster's tile range meeting a
+// sequence), at most B + G - 1 of them.
+size_t decode_ws_bytes(int H, int32_t B) {
+  const size_t slots = static_cast<size_t>(B + decode_clusters() - 1) * H;
   return slots * kLatent * sizeof(float) + slots * 2 * sizeof(float);
 }
 
@@ -127,15 +115,15 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
     return MLA_ERR_MISALIGNED;
   if (B < 1 || max_len < 1 || n_rows < 1) return MLA_ERR_INVALID_ARG;
   if (n_rows > INT32_MAX) return MLA_ERR_UNSUPPORTED;
-  if (B > 65535 || static_cast<int64_t>(B) * decode_plan(max_len).n_split > (1 << 30)) return MLA_ERR_UNSUPPORTED;
-  const size_t need = decode_ws_bytes(dims->n_head, B, max_len);
+  if (B > 65535) return MLA_ERR_UNSUPPORTED;
+  const size_t need = decode_ws_bytes(dims->n_head, B);
   if (workspace == nullptr || ws_bytes < need) return MLA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MLA_ERR_MISALIGNED;
   int* err = nullptr;
   cudaError_t e = error_word(&err);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  const DecodePlan plan = decode_plan(max_len);
-  const size_t slots = static_cast<size_t>(B) * plan.n_split * dims->n_head;
+  const int G = decode_clusters();
+  const size_t slots = static_cast<size_t>(B + G - 1) * dims->n_head;
   AttnTcArgs a = {};
   a.q_lat = q_lat;
   a.q_pe = q_pe;
@@ -148,14 +136,13 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.scale_log2 = dims->scale * kLog2eF;
   a.seq_start = seq_start;
   a.seq_len = seq_len;
-  a.n_split = plan.n_split;
-  a.chunk = plan.chunk;
+  a.n_seq = B;
   a.ws_o = static_cast<float*>(workspace);
   a.ws_ml = a.ws_o + slots * kLatent;
   a.err = err;
   a.wait_us = kDefaultWaitUs;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = launch_attn_tc(a, q8, true, B * plan.n_split, st);
+  e = launch_attn_tc(a, q8, true, G, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   CombineArgs c = {};
   c.ws_o = a.ws_o;
@@ -164,8 +151,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   c.o_lat = o_lat;
   c.B = B;
   c.n_head = dims->n_head;
-  c.n_split = plan.n_split;
-  c.chunk = plan.chunk;
+  c.n_clusters = G;
   return to_status(launch_combine(c, st));
 }
 
@@ -220,7 +206,7 @@ int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q
 
 size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_len) {
   if (check_dims(dims) != MLA_OK || B < 1 || max_len < 1) return 0;
-  return decode_ws_bytes(dims->n_head, B, max_len);
+  return decode_ws_bytes(dims->n_head, B);
 }
 
 int mla_attn_decode(const mla_dims* dims, const void* q_lat, const void* q_pe, const void* kv, int64_t n_rows,

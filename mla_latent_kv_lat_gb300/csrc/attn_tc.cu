@@ -57,41 +57,55 @@ constexpr int kOffRope = kOffLat + kLatStages * kLatStage;
 constexpr int kOffP = kOffRope + kRopeStages * kChunk;
 constexpr int kOffX = kOffP + kPBytes;
 constexpr int kOffAux = kOffX + 2 * kXBytes;
-// Softmax threads per query row: each takes 64 / kTpr keys of every tile.
-// Prefill runs four (sixteen softmax warps, more latency hidden per SM
-// sub-partition); decode two, leaving registers to its producer warps.
-__host__ __device__ constexpr int tpr(bool decode) { return decode ? 2 : 2; }
+// Two softmax threads per query row, each taking 32 keys of every tile (the
+// code is written for kTpr threads per row; one and four measured slower).
+constexpr int kTpr = 2;
 constexpr int kMaxTpr = 2, kMaxSoftmaxWarps = 4 * kMaxTpr;
 // row maxima [tile parity][thread of row][row], row sums [thread of row][row],
-// failure flags [tile parity][warp]
-// plus, for the epilogue warps, the row sums [item parity][row]
+// the row sums handed to the epilogue warps [item parity][row], failure
+// flags [tile parity][warp]
 constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows + 2 * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
 constexpr int kOffBar = kOffAux + kAuxBytes;
-constexpr int kSmem = 1024 + kOffBar + 256;
+constexpr int kBarBytes = 512;
+constexpr int kSmem = 1024 + kOffBar + kBarBytes;
 constexpr int kProducerWarps = 7;
 constexpr int kProducerThreads = kProducerWarps * 32;
-__host__ __device__ constexpr int softmax_warps(bool decode) { return 4 * tpr(decode); }
-// Loader warps: one TMA warp (prefill) or the producers (decode).
-__host__ __device__ constexpr int loader_warps(bool decode) { return decode ? kProducerWarps : 1; }
-// Prefill has four more warps (one per TMEM lane quadrant) that load each
-// item's Q into tensor memory as soon as the previous item's last score MMA
-// has completed, and write each item's output once its last P.V has: the
-// softmax warps go straight from one item's last tile to the next item's
-// first.  Decode has no registers to spare for them; its softmax warps do both.
-__host__ __device__ constexpr int epi_warps(bool decode) { return decode ? 0 : 4; }
-__host__ __device__ constexpr int loader_warp(bool decode) { return softmax_warps(decode) + epi_warps(decode); }
-__host__ __device__ constexpr int mma_warp(bool decode) { return loader_warp(decode) + loader_warps(decode); }
-// Prefill issues the score MMAs and the P.V MMAs from two warps, so that a
-// score tile waiting for its cache tile never holds back a P.V; decode has no
-// warp to spare and issues both from one.
-__host__ __device__ constexpr int mma_warps(bool decode) { return decode ? 1 : 2; }
-__host__ __device__ constexpr int threads(bool decode) { return (mma_warp(decode) + mma_warps(decode)) * 32; }
+constexpr int kConvWarps = 2;
+// bf16 decode: the two converter warps and the four epilogue warps convert
+// each tile (the epilogue warps have little else to do in decode).
+constexpr int kConvThreads = (kConvWarps + 4) * 32;
+// Warp roles, in this order:
+//   softmax (8) | epilogue (4; not for the q8_0 decode) | loader | MMA issue
+// The epilogue warps (one per TMEM lane quadrant) load each item's Q into
+// tensor memory as soon as the previous item's last score MMA has completed
+// and write each item's output once its last P.V has, so the softmax warps go
+// straight from one item's last tile to the next item's first.
+// Loader: prefill, one TMA warp (the cache is staged as fp16 beforehand);
+// bf16 decode, one TMA warp plus two warps converting each tile to fp16 in
+// place; q8_0 decode, seven producer warps that load, dequantise and store.
+// MMA issue: prefill, one warp for the score MMAs and one for P.V, so that a
+// score tile waiting for its cache tile never holds back a P.V; decode, one.
+__host__ __device__ constexpr int softmax_warps(bool, bool) { return 4 * kTpr; }
+__host__ __device__ constexpr int epi_warps(bool q8, bool decode) { return decode && q8 ? 0 : 4; }
+__host__ __device__ constexpr int loader_warps(bool q8, bool decode) {
+  return !decode ? 1 : (q8 ? kProducerWarps : 1 + kConvWarps);
+}
+__host__ __device__ constexpr int loader_warp(bool q8, bool decode) {
+  return softmax_warps(q8, decode) + epi_warps(q8, decode);
+}
+__host__ __device__ constexpr int mma_warp(bool q8, bool decode) {
+  return loader_warp(q8, decode) + loader_warps(q8, decode);
+}
+__host__ __device__ constexpr int mma_warps(bool, bool decode) { return decode ? 1 : 2; }
+__host__ __device__ constexpr int threads(bool q8, bool decode) {
+  return (mma_warp(q8, decode) + mma_warps(q8, decode)) * 32;
+}
 // Registers per thread: warps go to the four SM sub-partitions in turn, and
 // each sub-partition's 16384 registers are shared by its warps (allocated in
-// steps of 8 a thread).  Decode (16 warps): 128.
-__host__ __device__ constexpr int max_regs(bool decode) {
-  return (16384 / (((threads(decode) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
-             ? 248 : (16384 / (((threads(decode) / 32 + 3) / 4) * 32)) / 8 * 8;
+// steps of 8 a thread): 15 or 16 warps -> 128.
+__host__ __device__ constexpr int max_regs(bool q8, bool decode) {
+  return (16384 / (((threads(q8, decode) / 32 + 3) / 4) * 32)) / 8 * 8 > 255
+             ? 248 : (16384 / (((threads(q8, decode) / 32 + 3) / 4) * 32)) / 8 * 8;
 }
 // TMEM columns: Q latent half (A operand, 256 fp16 = 128 cols), two fp32 score
 // buffers of 64 columns, the fp32 output half (256 cols).
@@ -101,6 +115,7 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 256 in fp
 
 struct Bars {
   uint64_t lat_full[kLatStages];
+  uint64_t lat_tma[kLatStages];   // bf16 decode: the TMA tile has landed (before conversion)
   uint64_t lat_empty[kLatStages];
   uint64_t rope_full[kRopeStages];
   uint64_t rope_empty[kRopeStages];
@@ -117,7 +132,7 @@ struct Bars {
   uint64_t l_ready[2];   // arrival per item (prefill), by item parity: row sums in aux
   uint32_t tmem;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 static_assert(kSmem <= 232448, "shared memory");
 
 MLA_DEVINL bool wait_all(uint64_t* bar, uint32_t parity, const AttnTcArgs& a) {
@@ -224,58 +239,134 @@ struct Item {
   int n_tiles;
 };
 
-template <bool kDecode>
-MLA_DEVINL Item item_at(const AttnTcArgs& a, int idx) {
+// Prefill: row tile `item` (the snake order over G clusters picks them).
+MLA_DEVINL Item prefill_item(const AttnTcArgs& a, int idx) {
   Item it;
-  if constexpr (kDecode) {
-    const int b = idx / a.n_split, s = idx % a.n_split;
-    const int len = a.seq_len[b];
-    const int lo = s * a.chunk;
-    it.key_base = a.seq_start[b] + lo;
-    it.kend = lo < len ? min(len - lo, a.chunk) : 0;
-    it.nvalid = a.n_head;
-    it.qrow0 = static_cast<int64_t>(b) * a.n_head;
-    it.slot0 = static_cast<int64_t>(idx) * a.n_head;
-  } else {
-    const int item = a.n_items - 1 - idx;     // long prefill rows (late tokens) first
-    const int64_t rho0 = static_cast<int64_t>(item) * kRows;
-    it.nvalid = static_cast<int>(min(static_cast<int64_t>(kRows), a.n_qrows - rho0));
-    it.kend = a.q_pos0 + static_cast<int>((rho0 + it.nvalid - 1) / a.n_head) + 1;
-    it.key_base = 0;
-    it.qrow0 = rho0;
-    it.slot0 = 0;
-  }
+  const int item = a.n_items - 1 - idx;       // long prefill rows (late tokens) first
+  const int64_t rho0 = static_cast<int64_t>(item) * kRows;
+  it.nvalid = static_cast<int>(min(static_cast<int64_t>(kRows), a.n_qrows - rho0));
+  it.kend = a.q_pos0 + static_cast<int>((rho0 + it.nvalid - 1) / a.n_head) + 1;
+  it.key_base = 0;
+  it.qrow0 = rho0;
+  it.slot0 = 0;
   it.n_tiles = (it.kend + kBK - 1) / kBK;
   return it;
 }
 
+// This cluster's items in order.  Prefill: one row tile per round (snake
+// order).  Decode: the pieces of the cluster's tile range (see
+// decode_cluster_lo), one per sequence it meets.  (Two types, so that the
+// prefill warps carry no decode state in registers.)
+template <bool kDecode>
+struct ItemIter;
+
+template <>
+struct ItemIter<false> {
+  const AttnTcArgs* a;
+  int c, g, r;
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
+    a = &args; c = cluster; g = clusters; r = 0;
+  }
+  MLA_DEVINL bool next(Item& it) {
+    while (r * g < a->n_items) {
+      const int idx = round_item(c, g, r++);
+      if (idx < a->n_items) {
+        it = prefill_item(*a, idx);
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+template <>
+struct ItemIter<true> {
+  const AttnTcArgs* a;
+  int c, g;
+  int b;                       // next sequence
+  int64_t lo, hi, S;           // cluster tile range, first tile of sequence b
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
+    a = &args; c = cluster; g = clusters; b = 0; S = 0;
+    int64_t T = 0;
+    for (int q = 0; q < a->n_seq; ++q) T += decode_seq_tiles(a->seq_len[q]);
+    lo = decode_cluster_lo(T, g, c);
+    hi = decode_cluster_lo(T, g, c + 1);
+  }
+  MLA_DEVINL bool next(Item& it) {
+    while (b < a->n_seq && S < hi) {
+      const int32_t len = a->seq_len[b];
+      const int64_t tb = decode_seq_tiles(len);
+      const int64_t p_lo = max(lo, S), p_hi = min(hi, S + tb);
+      const int bb = b;
+      const int64_t s0 = S;
+      S += tb;
+      ++b;
+      if (p_lo >= p_hi) continue;
+      const int64_t k0 = (p_lo - s0) * kBK;          // first key of the piece in its sequence
+      it.key_base = a->seq_start[bb] + k0;
+      it.kend = static_cast<int>(min(static_cast<int64_t>(len) - k0, (p_hi - p_lo) * kBK));
+      it.nvalid = a->n_head;
+      it.qrow0 = static_cast<int64_t>(bb) * a->n_head;
+      it.slot0 = static_cast<int64_t>(bb + c) * a->n_head;
+      it.n_tiles = static_cast<int>(p_hi - p_lo);
+      return true;
+    }
+    return false;
+  }
+};
+
 // Walks this cluster's tiles in order across its items.
 template <bool kDecode>
 struct TileCursor {
-  const AttnTcArgs* a;
-  int c, g, r;        // cluster, cluster count, round
+  ItemIter<kDecode> iter;
   Item it;
   int t;              // tile within the item
-  MLA_DEVINL bool done() const { return r * g >= a->n_items; }
-  MLA_DEVINL void load_round() {
-    const int idx = round_item(c, g, r);
-    if (idx < a->n_items) it = item_at<kDecode>(*a, idx); else it.n_tiles = 0;
-  }
+  bool more;
   MLA_DEVINL void skip_empty() {
-    while (!done() && t >= it.n_tiles) {
-      ++r;
+    while (more && t >= it.n_tiles) {
+      more = iter.next(it);
       t = 0;
-      if (!done()) load_round();
     }
   }
   MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
-    a = &args; c = cluster; g = clusters; r = 0; t = 0;
-    if (!done()) load_round();
+    iter.init(args, cluster, clusters);
+    t = 0;
+    more = iter.next(it);
     skip_empty();
   }
-  MLA_DEVINL bool valid() const { return !done(); }
+  MLA_DEVINL bool valid() const { return more; }
   MLA_DEVINL void next() { ++t; skip_empty(); }
 };
+
+// bf16 -> fp16 in place of this thread's share (thread ct of kConvThreads) of
+// a landed latent tile.  A 16-byte unit holds 8 consecutive values of one key,
+// so the swizzle does not matter; exact over fp16's normal range.
+MLA_DEVINL void convert_share(uint8_t* stage, int ct) {
+  constexpr int kUnits = kLatStage / 16;
+  constexpr int kPer = (kUnits + kConvThreads - 1) / kConvThreads;
+  uint4* st = reinterpret_cast<uint4*>(stage);
+  uint4 v[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m)
+    if (ct + m * kConvThreads < kUnits) v[m] = st[ct + m * kConvThreads];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m)
+    if (ct + m * kConvThreads < kUnits) st[ct + m * kConvThreads] = bf16x8_to_f16x8(v[m]);
+}
+
+// L2 prefetch of one decode tile's cache rows (the rows of both CTAs' parts).
+constexpr int kPrefetchTiles = 8;
+template <bool kDecode>
+MLA_DEVINL void prefetch_tile_rows(const AttnTcArgs& a, const TileCursor<kDecode>& c) {
+  const int64_t row0 = c.it.key_base + static_cast<int64_t>(c.t) * kBK;
+  const int64_t rows = min(static_cast<int64_t>(kBK), a.n_rows - row0);
+  if (rows <= 0) return;
+  if (a.kv != nullptr) {
+    tc::prefetch_l2(static_cast<const uint16_t*>(a.kv) + row0 * kRow, static_cast<uint32_t>(rows * kRow * 2));
+  } else {
+    tc::prefetch_l2(a.kv_q + row0 * kRow, static_cast<uint32_t>(rows * kRow));
+  }
+}
 
 // kRope: this producer writes the RoPE ring (q8_0 cache, rank 0).  With a bf16
 // cache the RoPE tiles come by TMA, issued when `tma_rope` is set (rank 0).
@@ -288,12 +379,23 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   TileCursor<true> cur;
   cur.init(a, first, stride);
   if (!cur.valid()) return;
+  // One thread keeps the rows of the tiles kPrefetchTiles ahead on their way into L2.
+  TileCursor<true> ahead = cur;
+  const bool pf = pt == 0 && rank == 0;
+  for (int d = 0; d < kPrefetchTiles && ahead.valid(); ++d) {
+    if (pf) prefetch_tile_rows(a, ahead);
+    ahead.next();
+  }
   P x, y;
   int64_t cur_row = cur.it.key_base + static_cast<int64_t>(cur.t) * kBK;
   x.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
   cur.next();
   // Tile u+1's loads are in flight while tile u is converted and stored.
   auto step = [&](int u, P& now, P& nxt) -> bool {
+    if (ahead.valid()) {
+      if (pf) prefetch_tile_rows(a, ahead);
+      ahead.next();
+    }
     const bool more = cur.valid();
     const int64_t nxt_row = more ? cur.it.key_base + static_cast<int64_t>(cur.t) * kBK : 0;
     if (more) {
@@ -329,15 +431,14 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
 // ---------------------------------------------------------------------------
 // kDecode = false: prefill from the fp16 staging copy (kQ8 unused).
 template <bool kQ8, bool kDecode>
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, AttnTcArgs a) {
   // fp16 RoPE operands (prefill staging copy, q8_0 decode) or bf16 (bf16 decode).
   constexpr bool kRopeF16 = kQ8 || !kDecode;
-  constexpr int kMmaWarp = mma_warp(kDecode);
-  constexpr bool kEpi = epi_warps(kDecode) > 0;
-  constexpr int kLoaderWarp = loader_warp(kDecode);
-  constexpr int kSoftmaxWarps = softmax_warps(kDecode);
-  constexpr int kTpr = tpr(kDecode);
+  constexpr int kMmaWarp = mma_warp(kQ8, kDecode);
+  constexpr bool kEpi = epi_warps(kQ8, kDecode) > 0;
+  constexpr int kLoaderWarp = loader_warp(kQ8, kDecode);
+  constexpr int kSoftmaxWarps = softmax_warps(kQ8, kDecode);
   constexpr int kKpt = kBK / kTpr;          // keys of each tile per softmax thread: 32 or 16
   constexpr int kUpt = kKpt / 8;            // the same as 16-byte units of fp16: 4 or 2
   constexpr int kOpt = 256 / kTpr;          // output columns (of this CTA's half) per thread: 128 or 64
@@ -365,7 +466,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
   // ---- setup -----------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLatStages; ++i) {
-      mbar_init(&B.lat_full[i], kDecode ? kProducerThreads : 1);
+      mbar_init(&B.lat_full[i], !kDecode ? 1 : (kQ8 ? kProducerThreads : kConvThreads));   // converters + epilogue warps
+      mbar_init(&B.lat_tma[i], 1);
       mbar_init(&B.lat_empty[i], 1);
     }
     for (int i = 0; i < kRopeStages; ++i) {
@@ -467,12 +569,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     uint32_t own[kKpt / 2], nxt[kKpt / 2];
     int u0 = 0;                                 // this item's first tile, counted across items
     int k = 0;                                  // items done
+    ItemIter<kDecode> items;
+    items.init(a, first, stride);
+    Item it;
 #pragma unroll 1
-    for (int rnd = 0; rnd * stride < a.n_items; ++rnd) {
-      const int idx = round_item(first, stride, rnd);
-      if (idx >= a.n_items) continue;
-      const Item it = item_at<kDecode>(a, idx);
-      if (it.n_tiles == 0) continue;
+    while (items.next(it)) {
       const bool rvalid = i < it.nvalid;
       const int64_t qrow = it.qrow0 + i;
       int lim;                                  // last visible key index (item-relative)
@@ -633,7 +734,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
 #pragma unroll
         for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
         if (hh == 0) aux_lrow[(k & 1) * kRows + i] = l_row;
-        if (rank == 0 && hh == 0 && rvalid && a.lse != nullptr) a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
+        if (rank == 0 && hh == 0 && rvalid) {
+          if constexpr (kDecode) {
+            a.ws_ml[2 * (it.slot0 + i)] = m_run;
+            a.ws_ml[2 * (it.slot0 + i) + 1] = l_row;
+          } else if (a.lse != nullptr) {
+            a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
+          }
+        }
         mbar_arrive(&B.l_ready[k & 1]);
       } else {
         // Decode: O / l -> the fp32 partials, with the running max and sum.
@@ -673,6 +781,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       ++k;
     }
   } else if (kEpi && warp < kLoaderWarp) {
+    if constexpr (!kDecode) {
     // ======================= Q loading and epilogue (prefill) ==================
     // Warp 8+q serves TMEM lane quadrant q: thread = query row i, the whole
     // 256-column half of the row.  Per item k: once item k-1's last score MMA
@@ -716,7 +825,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     for (int rnd = 0; ok && rnd * stride < a.n_items; ++rnd) {
       const int idx = round_item(first, stride, rnd);
       if (idx >= a.n_items) continue;
-      const Item it = item_at<kDecode>(a, idx);
+      const Item it = prefill_item(a, idx);
       if (it.n_tiles == 0) continue;
       if (k > 0) ok = wait_all(&B.q_free, (k - 1) & 1, a);
       if (!ok) break;
@@ -754,7 +863,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       if (lane == 0 && q4 == 0 && (rnd + 1) * stride < a.n_items) {
         const int nidx = round_item(first, stride, rnd + 1);
         if (nidx < a.n_items) {
-          const Item nx = item_at<kDecode>(a, nidx);
+          const Item nx = prefill_item(a, nidx);
           if (rank == 0)
             tc::prefetch_l2(static_cast<const uint16_t*>(a.q_lat) + nx.qrow0 * kLatent,
                             static_cast<uint32_t>(nx.nvalid) * kLatent * 2);
@@ -768,24 +877,155 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       ++k;
     }
     if (ok && k > 0) epilogue(prev, k - 1);
+    } else {
+    // ============ Q loading, tile conversion and epilogue (bf16 decode) ========
+    // As for prefill, per item (piece): Q once the previous item's last score
+    // MMA has completed, the fp32 partial once its last P.V has.  In between,
+    // these warps convert their share of every tile to fp16 (see
+    // convert_share): in decode they have little else to do.  (A separate
+    // copy of the prefill code: sharing it cost the prefill kernel ~10%.)
+    const int q4 = warp & 3;
+    const int i = q4 * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    bool ok = true;
+    auto epilogue = [&](const Item& pv, int kk) {
+      ok = ok && wait_all(&B.o_ready, kk & 1, a);
+      ok = ok && wait_all(&B.l_ready[kk & 1], (kk >> 1) & 1, a);
+      if (!ok) return;
+      tc::fence_after_sync();
+      const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
+      const bool valid = i < pv.nvalid;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t o[32];
+        tc::tmem_ld32(tmem + lanes + kTmO + 32 * c, o);
+        tc::tmem_ld_wait();
+        if (!valid) continue;
+        // fp32 partial of this piece, normalised by its own sum
+        uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (pv.slot0 + i) * kLatent + 256 * rank + 32 * c);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          dst[v] = make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * inv),
+                              __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
+                              __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
+                              __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&B.o_free);
+    };
+    // Q of item k -> TMEM / smem, once item k-1's last score MMA has completed;
+    // `peek` is the item iterator positioned after `it` (for the L2 prefetch).
+    auto q_load = [&](const Item& it, int k, const ItemIter<kDecode>& peek_from) {
+      if (k > 0) ok = ok && wait_all(&B.q_free, (k - 1) & 1, a);
+      if (!ok) return;
+      tc::fence_after_sync();
+      const bool rvalid = i < it.nvalid;
+      const int64_t qrow = it.qrow0 + i;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_lat) + qrow * kLatent +
+                                                        256 * rank);
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {          // two rounds of 16 loads (128 dims each)
+        uint32_t r[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = rvalid ? __ldg(src + (2 * h2 + c) * 8 + v) : make_uint4(0, 0, 0, 0);
+            r[c][4 * v] = x.x; r[c][4 * v + 1] = x.y; r[c][4 * v + 2] = x.z; r[c][4 * v + 3] = x.w;
+          }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tc::tmem_st32(tmem + lanes + kTmQ + 32 * (2 * h2 + c), r[c]);
+      }
+      tc::tmem_st_wait();
+      if (rank == 0) {                          // RoPE query part -> smem (fp16, or bf16 for the bf16 decode)
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
+        uint4 qpe[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) st_unit(sQr, i, v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+        tc::fence_proxy_async();
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&B.q_ready);
+      // Bring the next item's queries into L2 meanwhile.
+      if (lane == 0 && q4 == 0) {
+        ItemIter<kDecode> peek = peek_from;
+        Item nx;
+        if (peek.next(nx)) {
+          if (rank == 0)
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_lat) + nx.qrow0 * kLatent,
+                            static_cast<uint32_t>(nx.nvalid) * kLatent * 2);
+          else
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_pe) + nx.qrow0 * kRope,
+                            static_cast<uint32_t>(nx.nvalid) * kRope * 2);
+        }
+      }
+    };
+    Item prev;
+    int k = 0;
+    {
+      // Conversion share 64 + 32 q4 + lane; at an item's first tile, its Q
+      // first, then the tile, then the previous item's epilogue (its P.V has
+      // to finish anyway before the new item's first P.V may start).
+      const int ct = 64 + q4 * 32 + lane;
+      TileCursor<kDecode> cur;
+      cur.init(a, first, stride);
+#pragma unroll 1
+      for (int u = 0; ok && cur.valid(); ++u, cur.next()) {
+        const bool first_tile = cur.t == 0;
+        if (first_tile) q_load(cur.it, k, cur.iter);
+        const int ls = u % kLatStages;
+        ok = ok && wait_all(&B.lat_tma[ls], (u / kLatStages) & 1, a);
+        if (!ok) break;
+        convert_share(sLat + ls * kLatStage, ct);
+        tc::fence_proxy_async();
+        mbar_arrive(&B.lat_full[ls]);
+        if (first_tile) {
+          if (k > 0) epilogue(prev, k - 1);
+          prev = cur.it;
+          ++k;
+        }
+      }
+    }
+    if (ok && k > 0) epilogue(prev, k - 1);
+    }
   } else if (warp < kMmaWarp) {
     // ============================ loader =======================================
     const int pt = threadIdx.x - kLoaderWarp * 32;
-    if constexpr (!kDecode) {
-      // One thread: each tile's four 64-dim latent chunks of this CTA's half
-      // (and, on rank 0, the RoPE part) by TMA, as soon as the stage is free.
+    if constexpr (!kDecode || !kQ8) {
       if (pt == 0) {
-        TileCursor<false> cur;
+        // One thread: each tile's four 64-dim latent chunks of this CTA's half
+        // (and, on rank 0, the RoPE part) by TMA, as soon as the stage is free.
+        // Prefill reads the fp16 staging copy (the tile is ready on arrival);
+        // the bf16 decode reads the cache itself and the tile is converted
+        // before the MMAs may read it.
+        uint64_t* landed = kDecode ? B.lat_tma : B.lat_full;
+        TileCursor<kDecode> cur, ahead;
         cur.init(a, first, stride);
+        // Decode reads every cache row from HBM once: keep the rows of the
+        // tiles kPrefetchTiles ahead on their way into L2, so that a stage's
+        // TMA, issued only when its previous tile is done, finds them there.
+        if (kDecode) {
+          ahead = cur;
+          for (int d = 0; d < kPrefetchTiles && ahead.valid(); ++d) {
+            if (rank == 0) prefetch_tile_rows(a, ahead);
+            ahead.next();
+          }
+        }
         for (int u = 0; cur.valid(); ++u, cur.next()) {
           const int ls = u % kLatStages, rs = u % kRopeStages;
           const int key = static_cast<int>(cur.it.key_base) + cur.t * kBK;
+          if (kDecode && ahead.valid()) {
+            if (rank == 0) prefetch_tile_rows(a, ahead);
+            ahead.next();
+          }
           if (u >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((u / kLatStages) - 1) & 1, a.wait_us, a.err))
             break;
-          mbar_arrive_expect_tx(&B.lat_full[ls], kLatStage);
+          mbar_arrive_expect_tx(&landed[ls], kLatStage);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            tc::tma_load_3d(sLat + ls * kLatStage + c * kChunk, &tm_cache, &B.lat_full[ls], 256 * rank + 64 * c, key, 0);
+            tc::tma_load_3d(sLat + ls * kLatStage + c * kChunk, &tm_cache, &landed[ls], 256 * rank + 64 * c, key, 0);
           if (rank == 0) {
             if (u >= kRopeStages &&
                 !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
@@ -794,15 +1034,26 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
             tc::tma_load_3d(sRope + rs * kChunk, &tm_cache, &B.rope_full[rs], kLatent, key, 0);
           }
         }
+      } else if (kDecode && pt >= 32) {
+        // bf16 decode: two warps convert each landed latent tile to fp16 in
+        // place (exact over fp16's normal range).  A 16-byte unit holds 8
+        // consecutive values of one key, so the swizzle does not matter.
+        const int ct = pt - 32;                 // 0..63; the epilogue warps are 64..191
+        TileCursor<kDecode> cur;
+        cur.init(a, first, stride);
+        for (int u = 0; cur.valid(); ++u, cur.next()) {
+          const int ls = u % kLatStages;
+          if (!wait_all(&B.lat_tma[ls], (u / kLatStages) & 1, a)) break;
+          convert_share(sLat + ls * kLatStage, ct);
+          tc::fence_proxy_async();
+          mbar_arrive(&B.lat_full[ls]);
+        }
       }
-    } else if constexpr (kQ8) {
+    } else {
       if (rank == 0)
         run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, first, stride);
       else
         run_producer<true, false>(&tm_cache, a, B, sLat, sRope, 1, false, pt, first, stride);
-    } else {
-      run_producer<false, false>(&tm_cache, a, B, sLat, sRope, static_cast<int>(rank), rank == 0, pt, first,
-                                 stride);
     }
   } else {
     // ============================== MMA issue ==================================
@@ -858,16 +1109,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
       tc::mma_commit_warp(&B.pv_done);
       return true;
     };
-    if constexpr (mma_warps(kDecode) == 2) {
+    if constexpr (mma_warps(kQ8, kDecode) == 2) {
       // Each stream in order, each as soon as its operands are ready (the
       // score MMAs are bounded by the two score buffers, so they run at most
       // three tiles ahead of P.V).
       int u = 0, k = 0;
-      for (int r = 0; ok && r * stride < a.n_items; ++r) {
-        const int idx = round_item(first, stride, r);
-        if (idx >= a.n_items) continue;
-        const Item it = item_at<kDecode>(a, idx);
-        if (it.n_tiles == 0) continue;
+      ItemIter<kDecode> items;
+      items.init(a, first, stride);
+      Item it;
+      while (ok && items.next(it)) {
         if (warp == kMmaWarp) {
           // Q of item k in TMEM (the k-th arrival on q_ready).
           ok = wait_all(&B.q_ready, k & 1, a);
@@ -884,22 +1134,27 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kDecode))
     } else {
       // One warp: scores run up to three tiles ahead of P.V within an item; at
       // an item boundary the next item's first scores wait until its Q is in
-      // TMEM, which the softmax loads only after it has produced every P of
-      // the current item, so they are issued after the current item's last P.V.
+      // TMEM, which is loaded only after the current item's last score MMA
+      // (epilogue warps) or after its last P (softmax warps), so they are
+      // issued after the current item's last P.V.
       int u = 0, k = 0;
-      for (int r = 0; ok && r * stride < a.n_items; ++r) {
-        const int idx = round_item(first, stride, r);
-        if (idx >= a.n_items) continue;
-        const Item it = item_at<kDecode>(a, idx);
-        if (it.n_tiles == 0) continue;
+      ItemIter<kDecode> items;
+      items.init(a, first, stride);
+      Item it;
+      while (ok && items.next(it)) {
         const int n = it.n_tiles;
         ok = wait_all(&B.q_ready, k & 1, a);
         tc::fence_after_sync();
         for (int t = 0; ok && t < 3 && t < n; ++t) ok = issue_qk(u + t);
+        if (ok && kEpi && n <= 3) tc::mma_commit_warp(&B.q_free);
         for (int t = 0; ok && t < n; ++t) {
           ok = issue_pv(u + t, t == 0, k);
-          if (ok && t + 3 < n) ok = issue_qk(u + t + 3);
+          if (ok && t + 3 < n) {
+            ok = issue_qk(u + t + 3);
+            if (ok && kEpi && t + 3 == n - 1) tc::mma_commit_warp(&B.q_free);
+          }
         }
+        if (ok && kEpi) tc::mma_commit_warp(&B.o_ready);
         u += n;
         ++k;
       }
@@ -920,13 +1175,15 @@ cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_cluster
   auto kern = attn_tc_kernel<kQ8, kDecode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(2 * n_clusters), threads(kDecode), kSmem, stream>>>(tm, a);
+  kern<<<dim3(2 * n_clusters), threads(kQ8, kDecode), kSmem, stream>>>(tm, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 int attn_tc_rows_per_item() { return kRows; }
+
+int decode_clusters() { return max(1, device_sm_count() / 2); }
 
 cudaError_t launch_attn_tc(const AttnTcArgs& args, bool q8, bool decode, int n_items, cudaStream_t stream) {
   if (n_items <= 0) return cudaSuccess;

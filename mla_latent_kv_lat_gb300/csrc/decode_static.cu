@@ -14,10 +14,10 @@
 
 namespace {
 
-// Maximum scratch: 32 MiB.  A decode needs B * ceil(max_len / 2048) * H * 2056
-// bytes of it (fp32 partial sums of 512 latent values plus a running max and
-// sum per head and split), e.g. B = 8 sequences of up to 16384 tokens at 128
-// heads use 16.8 MB.
+// Maximum scratch: 32 MiB.  A decode needs (B + G - 1) * H * 2056 bytes of it
+// (G = SM count / 2 clusters; per piece and head, fp32 partial sums of 512
+// latent values plus a running max and sum), e.g. B = 8 sequences at 128
+// heads on GB300 (G = 76) use 21.8 MB.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];

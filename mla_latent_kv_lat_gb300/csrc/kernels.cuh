@@ -7,12 +7,22 @@
 
 namespace mla {
 
+// Split-KV decode, evenly over G clusters: the 64-key tiles of all sequences,
+// in sequence order, form one run of T tiles, and cluster c takes tiles
+// [c*T/G, (c+1)*T/G).  Where a cluster's range meets a sequence is a piece; it
+// produces one partial result, in slot b + c (pieces are ordered by sequence,
+// then cluster, and each starts at a sequence or cluster boundary).  Every
+// cluster does the same number of tiles (to one), whatever the lengths.
+constexpr int kDecodeTile = 64;
+MLA_DEVINL int64_t decode_seq_tiles(int32_t len) { return (static_cast<int64_t>(len) + kDecodeTile - 1) / kDecodeTile; }
+MLA_DEVINL int64_t decode_cluster_lo(int64_t T, int G, int c) { return T * c / G; }
+
 struct CombineArgs {
   const float* ws_o;
   const float* ws_ml;
   const int32_t* seq_len;
   void* o_lat;
-  int B, n_head, n_split, chunk;
+  int B, n_head, n_clusters;
 };
 
 // C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: bf16 A, K=128, N=512,
@@ -45,10 +55,9 @@ struct AttnTcArgs {
   // decode
   const int64_t* seq_start;
   const int32_t* seq_len;
-  int n_split;
-  int chunk;
-  float* ws_o;              // fp32 [B * n_split][H][512] partial o_lat, normalised by its own sum
-  float* ws_ml;             // fp32 [B * n_split][H][2]   running max (log2 units) and sum
+  int n_seq;                // B
+  float* ws_o;              // fp32 [B + G - 1][H][512] partial o_lat per piece, normalised by its own sum
+  float* ws_ml;             // fp32 [B + G - 1][H][2]   running max (log2 units) and sum
   int* err;
   uint32_t wait_us;
   int n_items;              // set by launch_attn_tc
@@ -58,7 +67,11 @@ struct AttnTcArgs {
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
+// Prefill: n_items row tiles of 128.  Decode: n_items = number of clusters G
+// (the pieces are found on the device).
 cudaError_t launch_attn_tc(const AttnTcArgs& a, bool q8, bool decode, int n_items, cudaStream_t stream);
+// Clusters a decode launch uses (one per SM pair); its workspace holds B + G - 1 pieces.
+int decode_clusters();
 int attn_tc_rows_per_item();
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream);

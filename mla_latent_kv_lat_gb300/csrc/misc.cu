@@ -65,18 +65,31 @@ cudaError_t launch_wait_timeout_selftest(uint32_t wait_us, int* err, cudaStream_
 namespace {
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
   const int b = blockIdx.x / c.n_head, h = blockIdx.x % c.n_head;
-  const int64_t len = c.seq_len[b];
-  const int ns = static_cast<int>(min(static_cast<int64_t>(c.n_split), (len + c.chunk - 1) / c.chunk));
+  // This sequence's tiles [Sb, Eb) in the run of all sequences' tiles, and
+  // the clusters whose ranges meet it (one piece each, slot b + cluster).
+  int64_t T = 0, Sb = 0;
+  for (int q = 0; q < c.B; ++q) {
+    const int64_t t = decode_seq_tiles(c.seq_len[q]);
+    if (q < b) Sb += t;
+    T += t;
+  }
+  const int64_t Eb = Sb + decode_seq_tiles(c.seq_len[b]);
+  const int G = c.n_clusters;
+  int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Sb * G / max(T, static_cast<int64_t>(1))));
+  while (c0 > 0 && decode_cluster_lo(T, G, c0) > Sb) --c0;
+  while (c0 + 1 < G && decode_cluster_lo(T, G, c0 + 1) <= Sb) ++c0;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) {
-    const int64_t slot = (static_cast<int64_t>(b) * c.n_split + s) * c.n_head + h;
+  for (int cl = c0; cl < G && decode_cluster_lo(T, G, cl) < Eb; ++cl) {
+    if (decode_cluster_lo(T, G, cl + 1) <= decode_cluster_lo(T, G, cl)) continue;   // empty range
+    const int64_t slot = static_cast<int64_t>(b + cl) * c.n_head + h;
     M = fmaxf(M, c.ws_ml[2 * slot]);
   }
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int col = threadIdx.x * 4;
-  for (int s = 0; s < ns; ++s) {
-    const int64_t slot = (static_cast<int64_t>(b) * c.n_split + s) * c.n_head + h;
+  for (int cl = c0; cl < G && decode_cluster_lo(T, G, cl) < Eb; ++cl) {
+    if (decode_cluster_lo(T, G, cl + 1) <= decode_cluster_lo(T, G, cl)) continue;
+    const int64_t slot = static_cast<int64_t>(b + cl) * c.n_head + h;
     // partials are normalised by their own sum l_s: weight 2^(m_s - M) * l_s
     const float w = exp2f(c.ws_ml[2 * slot] - M) * c.ws_ml[2 * slot + 1];
     L += w;

@@ -89,11 +89,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_selftest_wait_timeout(0, None) == -1
 
 
-def test_workspace_size_grows_with_batch_and_length(lib):
+def test_workspace_size_grows_with_batch_not_length(lib):
+    # one partial per piece: at most B + G - 1 of H x 2056 bytes, G = clusters
     a = lib.mla_decode_workspace_size(_dims(128), 8, 4096)
     b = lib.mla_decode_workspace_size(_dims(128), 16, 4096)
     c = lib.mla_decode_workspace_size(_dims(128), 8, 65536)
-    assert 0 < a < b and a < c
+    assert 0 < a < b and a == c
+    assert b - a == 8 * 128 * 2056 and a % (128 * 2056) == 0
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):

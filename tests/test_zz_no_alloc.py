@@ -48,10 +48,12 @@ def test_static_scratch_decode_matches_workspace_decode():
         torch.cuda.synchronize()
         assert mla.mla_get_device_error() == 0
         assert_tol(out.float().cpu().numpy(), ref.float().cpu().numpy(), TOL_BF16, f"static decode {lengths}")
-    # 32 sequences of 32768 tokens at 128 heads need 134.7 MB of scratch: refused on the host
-    q_lat = torch.zeros(32, 128, 512, dtype=torch.float16, device="cuda")
-    q_pe = torch.zeros(32, 128, 64, dtype=torch.bfloat16, device="cuda")
+    # 64 sequences at 128 heads need more than 32 MiB of scratch: refused on the host
+    need = mla.mla_decode_workspace_size(128, 64, 32768)
+    assert need > 32 << 20
+    q_lat = torch.zeros(64, 128, 512, dtype=torch.float16, device="cuda")
+    q_pe = torch.zeros(64, 128, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mla.MLAError) as e:
-        mla.mla_attn_decode_static(q_lat, q_pe, kv, torch.zeros(32, dtype=torch.int64, device="cuda"),
-                                   torch.ones(32, dtype=torch.int32, device="cuda"), 32768, q_lat)
+        mla.mla_attn_decode_static(q_lat, q_pe, kv, torch.zeros(64, dtype=torch.int64, device="cuda"),
+                                   torch.ones(64, dtype=torch.int32, device="cuda"), 32768, q_lat)
     assert e.value.status == -4
