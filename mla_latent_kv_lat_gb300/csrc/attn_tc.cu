@@ -48,7 +48,7 @@ constexpr int kBK = 64;                      // keys per tile
 constexpr int kChunk = kBK * 128;            // 8 KB: 64 keys x 64 16-bit values
 constexpr int kLatStage = 4 * kChunk;        // 32 KB: this CTA's 256 latent dims
 constexpr int kLatStages = 4;
-constexpr int kRopeStages = 3;
+constexpr int kRopeStages = 2;   // a RoPE tile is done with long before its latent stage
 constexpr int kQRopeBytes = kRows * 128;     // 16 KB: 128 rows x 64 dims
 constexpr int kPBytes = kRows * 128;         // 16 KB: 128 rows x 64 keys fp16
 constexpr int kXBytes = kRows * kBK * 2;     // 16 KB: one exchange buffer (fp16 partial scores)
@@ -65,7 +65,11 @@ constexpr int kMaxTpr = 2, kMaxSoftmaxWarps = 4 * kMaxTpr;
 // the row sums handed to the epilogue warps [item parity][row], failure
 // flags [tile parity][warp]
 constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows + 2 * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
-constexpr int kOffBar = kOffAux + kAuxBytes;
+// Epilogue warps' output staging: 2 KB per warp (32 rows x 64 B), so that the
+// global stores leave as 64-byte row pieces, not 16-byte pieces of 32 rows.
+constexpr int kStgBytes = 4 * 2048;
+constexpr int kOffStg = kOffAux + kAuxBytes;
+constexpr int kOffBar = kOffStg + kStgBytes;
 constexpr int kBarBytes = 512;
 constexpr int kSmem = 1024 + kOffBar + kBarBytes;
 constexpr int kProducerWarps = 7;
@@ -354,6 +358,25 @@ MLA_DEVINL void convert_share(uint8_t* stage, int ct) {
     if (ct + m * kConvThreads < kUnits) st[ct + m * kConvThreads] = bf16x8_to_f16x8(v[m]);
 }
 
+// Store 64 bytes of each of a warp's 32 rows (lane = row, `w` = the row's four
+// 16-byte units) to dst_row0 + row * row_stride (bytes): through the warp's
+// 2 KB staging slice, so that each store instruction writes 8 rows x 64
+// contiguous bytes.  Units are XOR-swizzled by row pair (no bank conflicts).
+// Rows >= nrows are not stored.  Whole warp.
+MLA_DEVINL void store_rows64(uint8_t* stg, int lane, const uint4 (&w)[4], uint8_t* dst_row0, int64_t row_stride,
+                             int nrows) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = w[v];
+  __syncwarp();
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int rr = (lane >> 2) + 8 * m, part = lane & 3;
+    const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((part ^ ((rr >> 1) & 3)) << 4));
+    if (rr < nrows) *reinterpret_cast<uint4*>(dst_row0 + rr * row_stride + part * 16) = x;
+  }
+  __syncwarp();
+}
+
 // L2 prefetch of one decode tile's cache rows (the rows of both CTAs' parts).
 constexpr int kPrefetchTiles = 8;
 template <bool kDecode>
@@ -451,6 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
   uint8_t* sRope = sm + kOffRope;
   uint8_t* sP = sm + kOffP;
   uint8_t* sX = sm + kOffX;
+  uint8_t* sStg = sm + kOffStg;
   float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][kTpr][128] row maxima
   float* aux_l = aux_m + 2 * kMaxTpr * kRows;                   // [kTpr][128] row sums
   float* aux_lrow = aux_l + kMaxTpr * kRows;                    // [2][128] row sums for the epilogue warps
@@ -798,23 +822,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (!ok) return;
       tc::fence_after_sync();
       const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
-      const bool valid = i < pv.nvalid;
-      uint16_t* dst = static_cast<uint16_t*>(a.o_lat) + (pv.qrow0 + i) * kLatent + 256 * rank;
+      // This warp's 32 rows, 32 columns (64 B of fp16) per step, through its staging slice.
+      uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(a.o_lat) + (pv.qrow0 + q4 * 32) * kLatent +
+                                                256 * rank);
+      uint8_t* stg = sStg + (warp - kSoftmaxWarps) * 2048;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tmem + lanes + kTmO + 32 * c, o);
         tc::tmem_ld_wait();
-        if (!valid) continue;
+        uint4 w[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          uint4 w;
-          w.x = pack_f16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-          w.y = pack_f16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-          w.z = pack_f16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-          w.w = pack_f16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-          *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = w;
+          w[v].x = pack_f16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+          w[v].y = pack_f16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+          w[v].z = pack_f16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+          w[v].w = pack_f16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
         }
+        store_rows64(stg, lane, w, dst + c * 64, kLatent * 2, pv.nvalid - q4 * 32);
       }
       tc::fence_before_sync();
       mbar_arrive(&B.o_free);
@@ -894,21 +919,26 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (!ok) return;
       tc::fence_after_sync();
       const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
-      const bool valid = i < pv.nvalid;
+      // fp32 partial of this piece, normalised by its own sum: this warp's 32
+      // rows, 16 columns (64 B) per step, through its staging slice.
+      uint8_t* dst = reinterpret_cast<uint8_t*>(a.ws_o + (pv.slot0 + q4 * 32) * kLatent + 256 * rank);
+      uint8_t* stg = sStg + (warp - kSoftmaxWarps) * 2048;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tmem + lanes + kTmO + 32 * c, o);
         tc::tmem_ld_wait();
-        if (!valid) continue;
-        // fp32 partial of this piece, normalised by its own sum
-        uint4* dst = reinterpret_cast<uint4*>(a.ws_o + (pv.slot0 + i) * kLatent + 256 * rank + 32 * c);
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          dst[v] = make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * inv),
-                              __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
-                              __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
-                              __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint4 w[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            w[v] = make_uint4(__float_as_uint(__uint_as_float(o[16 * h2 + 4 * v]) * inv),
+                              __float_as_uint(__uint_as_float(o[16 * h2 + 4 * v + 1]) * inv),
+                              __float_as_uint(__uint_as_float(o[16 * h2 + 4 * v + 2]) * inv),
+                              __float_as_uint(__uint_as_float(o[16 * h2 + 4 * v + 3]) * inv));
+          store_rows64(stg, lane, w, dst + (32 * c + 16 * h2) * 4, kLatent * 4, pv.nvalid - q4 * 32);
+        }
       }
       tc::fence_before_sync();
       mbar_arrive(&B.o_free);
