@@ -391,6 +391,21 @@ MLA_DEVINL void prefetch_tile_rows(const AttnTcArgs& a, const TileCursor<kDecode
   }
 }
 
+// q8_0 tiles ahead, by one warp (lane = pt < 32): the codes as one bulk L2
+// prefetch, and the scales of the tile's rows in each of the 18 scale blocks
+// (lanes 0..17: the first and the last cache line of the block's run).
+MLA_DEVINL void prefetch_q8_tile(const AttnTcArgs& a, const TileCursor<true>& c, int lane) {
+  const int64_t row0 = c.it.key_base + static_cast<int64_t>(c.t) * kBK;
+  const int64_t rows = min(static_cast<int64_t>(kBK), a.n_rows - row0);
+  if (rows <= 0) return;
+  if (lane == 0) tc::prefetch_l2(a.kv_q + row0 * kRow, static_cast<uint32_t>(rows * kRow));
+  if (lane < kQ8Blocks) {
+    const uint16_t* d = a.kv_d + static_cast<int64_t>(lane) * a.ld_d + row0;
+    tc::prefetch_line_l2(d);
+    tc::prefetch_line_l2(d + rows - 1);
+  }
+}
+
 // kRope: this producer writes the RoPE ring (q8_0 cache, rank 0).  With a bf16
 // cache the RoPE tiles come by TMA, issued when `tma_rope` is set (rank 0).
 // Tile u counts this cluster's tiles across items.
@@ -404,9 +419,9 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   if (!cur.valid()) return;
   // One thread keeps the rows of the tiles kPrefetchTiles ahead on their way into L2.
   TileCursor<true> ahead = cur;
-  const bool pf = pt == 0 && rank == 0;
+  const bool pf = pt < 32 && rank == 0;
   for (int d = 0; d < kPrefetchTiles && ahead.valid(); ++d) {
-    if (pf) prefetch_tile_rows(a, ahead);
+    if (pf) prefetch_q8_tile(a, ahead, pt);
     ahead.next();
   }
   P x, y;
@@ -416,7 +431,7 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   // Tile u+1's loads are in flight while tile u is converted and stored.
   auto step = [&](int u, P& now, P& nxt) -> bool {
     if (ahead.valid()) {
-      if (pf) prefetch_tile_rows(a, ahead);
+      if (pf) prefetch_q8_tile(a, ahead, pt);
       ahead.next();
     }
     const bool more = cur.valid();
@@ -522,6 +537,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
   tc::cluster_sync();                 // peer barriers initialised before any remote arrival
   tc::fence_after_sync();
   const uint32_t tmem = B.tmem;
+  // Decode: the combine kernel, launched as a programmatic dependent, may be
+  // scheduled now; it waits for this grid's completion before reading.
+  if constexpr (kDecode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < kSoftmaxWarps) {
     // ======================= softmax / exchange / epilogue =====================

@@ -77,6 +77,12 @@ MLA_DEVINL float warp_sum(float v) {
   return v;
 }
 
+MLA_DEVINL long long warp_sum_i64(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier primitives (PTX ISA, "mbarrier" instructions), shared::cta scope.
 // ---------------------------------------------------------------------------

@@ -58,59 +58,128 @@ cudaError_t launch_wait_timeout_selftest(uint32_t wait_us, int* err, cudaStream_
 }
 
 // ---------------------------------------------------------------------------
-// Split-KV combine: merge the per-split partials of each (sequence, head) --
+// Split-KV combine: merge the per-piece partials of each (sequence, head) --
 // o_s normalised by its own sum l_s, running max m_s in log2 units -- by
-// log-sum-exp, and write o_lat in fp16.
+// log-sum-exp, and write o_lat in fp16.  One warp per (sequence, head), eight
+// heads per block; a lane holds 16 of the 512 columns (four 16-byte pieces,
+// 128 columns apart, so that each load instruction covers 512 contiguous
+// bytes), and the loads of up to four partials are in flight at once.
+// Launched as a programmatic dependent of the attention kernel: the block
+// sets up (the sequence's tile range) while the attention kernel drains, and
+// waits for its completion before the first read of the workspace.
 // ---------------------------------------------------------------------------
 namespace {
-__global__ void __launch_bounds__(128) combine_kernel(CombineArgs c) {
-  const int b = blockIdx.x / c.n_head, h = blockIdx.x % c.n_head;
-  // This sequence's tiles [Sb, Eb) in the run of all sequences' tiles, and
-  // the clusters whose ranges meet it (one piece each, slot b + cluster).
-  int64_t T = 0, Sb = 0;
-  for (int q = 0; q < c.B; ++q) {
-    const int64_t t = decode_seq_tiles(c.seq_len[q]);
-    if (q < b) Sb += t;
-    T += t;
+constexpr int kCombHeads = 8;
+
+__global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c) {
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // This sequence's tiles [Sb, Eb) in the run of all sequences' tiles.
+  __shared__ long long red[2][kCombHeads];
+  long long tb = 0, tt = 0;
+  for (int q = threadIdx.x; q < c.B; q += blockDim.x) {
+    const long long t = decode_seq_tiles(c.seq_len[q]);
+    tt += t;
+    if (q < b) tb += t;
+  }
+  tb = warp_sum_i64(tb);
+  tt = warp_sum_i64(tt);
+  if (lane == 0) {
+    red[0][warp] = tb;
+    red[1][warp] = tt;
+  }
+  __syncthreads();
+  int64_t Sb = 0, T = 0;
+#pragma unroll
+  for (int w = 0; w < kCombHeads; ++w) {
+    Sb += red[0][w];
+    T += red[1][w];
   }
   const int64_t Eb = Sb + decode_seq_tiles(c.seq_len[b]);
   const int G = c.n_clusters;
+  // The first cluster whose range meets [Sb, Eb): ranges are [lo(c), lo(c+1)).
   int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Sb * G / max(T, static_cast<int64_t>(1))));
   while (c0 > 0 && decode_cluster_lo(T, G, c0) > Sb) --c0;
   while (c0 + 1 < G && decode_cluster_lo(T, G, c0 + 1) <= Sb) ++c0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the attention kernel's partials are complete
+  const int h = blockIdx.y * kCombHeads + warp;
+  if (h >= c.n_head) return;
+  // Pass 1: the largest running max over the pieces (a lane per piece).
   float M = -INFINITY;
-  for (int cl = c0; cl < G && decode_cluster_lo(T, G, cl) < Eb; ++cl) {
-    if (decode_cluster_lo(T, G, cl + 1) <= decode_cluster_lo(T, G, cl)) continue;   // empty range
-    const int64_t slot = static_cast<int64_t>(b + cl) * c.n_head + h;
-    M = fmaxf(M, c.ws_ml[2 * slot]);
+  for (int x = c0 + lane; x < G && decode_cluster_lo(T, G, x) < Eb; x += 32) {
+    if (decode_cluster_lo(T, G, x + 1) <= decode_cluster_lo(T, G, x)) continue;   // empty range
+    M = fmaxf(M, c.ws_ml[2 * ((static_cast<int64_t>(b) + x) * c.n_head + h)]);
   }
+  M = warp_max(M);
+  // Pass 2: weights 2^(m_s - M) * l_s and the weighted partials.
   float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int col = threadIdx.x * 4;
-  for (int cl = c0; cl < G && decode_cluster_lo(T, G, cl) < Eb; ++cl) {
-    if (decode_cluster_lo(T, G, cl + 1) <= decode_cluster_lo(T, G, cl)) continue;
-    const int64_t slot = static_cast<int64_t>(b + cl) * c.n_head + h;
-    // partials are normalised by their own sum l_s: weight 2^(m_s - M) * l_s
-    const float w = exp2f(c.ws_ml[2 * slot] - M) * c.ws_ml[2 * slot + 1];
-    L += w;
-    const float4 o = *reinterpret_cast<const float4*>(c.ws_o + slot * kLatent + col);
-    acc.x = fmaf(w, o.x, acc.x);
-    acc.y = fmaf(w, o.y, acc.y);
-    acc.z = fmaf(w, o.z, acc.z);
-    acc.w = fmaf(w, o.w, acc.w);
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int cl = c0;
+  auto lo = [&](int x) { return decode_cluster_lo(T, G, x); };
+  while (cl < G && lo(cl) < Eb) {
+    // the next (up to) four non-empty pieces
+    int64_t slot[4];
+    bool has[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      while (cl < G && lo(cl) < Eb && lo(cl + 1) <= lo(cl)) ++cl;     // empty range
+      has[j] = cl < G && lo(cl) < Eb;
+      slot[j] = (static_cast<int64_t>(b) + cl) * c.n_head + h;
+      if (has[j]) ++cl;
+    }
+    float4 v[4][4];
+    float w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w[j] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (has[j]) {
+        const float4* src = reinterpret_cast<const float4*>(c.ws_o + slot[j] * kLatent) + lane;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[j][k] = src[32 * k];
+        w[j] = exp2f(c.ws_ml[2 * slot[j]] - M) * c.ws_ml[2 * slot[j] + 1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      L += w[j];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x = fmaf(w[j], v[j][k].x, acc[k].x);
+        acc[k].y = fmaf(w[j], v[j][k].y, acc[k].y);
+        acc[k].z = fmaf(w[j], v[j][k].z, acc[k].z);
+        acc[k].w = fmaf(w[j], v[j][k].w, acc[k].w);
+      }
+    }
   }
   const float inv = 1.f / L;
-  uint16_t* out = static_cast<uint16_t*>(c.o_lat) + (static_cast<int64_t>(b) * c.n_head + h) * kLatent + col;
-  uint2 pk;
-  pk.x = pack_f16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_f16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out) = pk;
+  uint2* out = reinterpret_cast<uint2*>(static_cast<uint16_t*>(c.o_lat) +
+                                        (static_cast<int64_t>(b) * c.n_head + h) * kLatent) + lane;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint2 pk;
+    pk.x = pack_f16x2(acc[k].x * inv, acc[k].y * inv);
+    pk.y = pack_f16x2(acc[k].z * inv, acc[k].w * inv);
+    out[32 * k] = pk;
+  }
 }
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream) {
-  combine_kernel<<<c.B * c.n_head, 128, 0, stream>>>(c);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c.B), static_cast<unsigned>((c.n_head + kCombHeads - 1) / kCombHeads));
+  cfg.blockDim = dim3(32 * kCombHeads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, c);
 }
 
 // ---------------------------------------------------------------------------

@@ -186,6 +186,11 @@ MLA_DEVINL void prefetch_l2(const void* p, uint32_t bytes) {
                : "memory");
 }
 
+// The cache line holding p into L2 (a hint; p any address inside an allocation).
+MLA_DEVINL void prefetch_line_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 MLA_DEVINL void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
