@@ -178,7 +178,8 @@ struct Producer {
   static constexpr int NUNITS = kBK * UPK;
   static constexpr int NU = (NUNITS + kProducerThreads - 1) / kProducerThreads;
   uint4 v[NU];
-  float d[kQ8 ? NU : 1];
+  uint32_t d[kQ8 ? NU : 1];   // raw fp16 scale bits: converted at store time, so no
+                               // instruction waits on the load before then
 
   MLA_DEVINL void load(const AttnTcArgs& a, int rank, int pt, int64_t key_base, int k0, int kend) {
 #pragma unroll
@@ -186,7 +187,7 @@ struct Producer {
       const int idx = pt + t * kProducerThreads;
       const int key = idx / UPK, cu = idx % UPK;
       v[t] = make_uint4(0, 0, 0, 0);
-      if constexpr (kQ8) d[t] = 0.f;
+      if constexpr (kQ8) d[t] = 0u;
       if (idx < NUNITS && k0 + key < kend) {
         const int64_t row = key_base + k0 + key;
         if constexpr (!kQ8) {
@@ -195,7 +196,7 @@ struct Producer {
         } else {
           const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + (cu - 16) * 16;
           v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
-          d[t] = __half2float(__ushort_as_half(__ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row)));
+          d[t] = __ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row);
         }
       }
     }
@@ -213,10 +214,11 @@ struct Producer {
         uint8_t* base = cu < 16 ? lat + (cu >> 2) * kChunk : rope;
         const int u = (cu & 3) * 2;
         uint4 lo, hi;
-        lo.x = i8x2_to_f16x2(v[t].x, 0, d[t]);  lo.y = i8x2_to_f16x2(v[t].x, 16, d[t]);
-        lo.z = i8x2_to_f16x2(v[t].y, 0, d[t]);  lo.w = i8x2_to_f16x2(v[t].y, 16, d[t]);
-        hi.x = i8x2_to_f16x2(v[t].z, 0, d[t]);  hi.y = i8x2_to_f16x2(v[t].z, 16, d[t]);
-        hi.z = i8x2_to_f16x2(v[t].w, 0, d[t]);  hi.w = i8x2_to_f16x2(v[t].w, 16, d[t]);
+        const float dt = __half2float(__ushort_as_half(static_cast<unsigned short>(d[t])));
+        lo.x = i8x2_to_f16x2(v[t].x, 0, dt);  lo.y = i8x2_to_f16x2(v[t].x, 16, dt);
+        lo.z = i8x2_to_f16x2(v[t].y, 0, dt);  lo.w = i8x2_to_f16x2(v[t].y, 16, dt);
+        hi.x = i8x2_to_f16x2(v[t].z, 0, dt);  hi.y = i8x2_to_f16x2(v[t].z, 16, dt);
+        hi.z = i8x2_to_f16x2(v[t].w, 0, dt);  hi.w = i8x2_to_f16x2(v[t].w, 16, dt);
         st_unit(base, key, u, lo);
         st_unit(base, key, u + 1, hi);
       }
