@@ -158,11 +158,6 @@ MLA_DEVINL uint4 bf16x8_to_f16x8(uint4 v) {
   return o;
 }
 
-MLA_DEVINL uint32_t i8x2_to_f16x2(uint32_t w, int sh, float d) {
-  const float a = static_cast<float>(static_cast<int8_t>((w >> sh) & 0xFF));
-  const float b = static_cast<float>(static_cast<int8_t>((w >> (sh + 8)) & 0xFF));
-  return pack_f16x2(a * d, b * d);
-}
 
 // ---------------------------------------------------------------------------
 // Producer: one 64-key tile of this CTA's cache part.
@@ -214,11 +209,11 @@ struct Producer {
         uint8_t* base = cu < 16 ? lat + (cu >> 2) * kChunk : rope;
         const int u = (cu & 3) * 2;
         uint4 lo, hi;
-        const float dt = __half2float(__ushort_as_half(static_cast<unsigned short>(d[t])));
-        lo.x = i8x2_to_f16x2(v[t].x, 0, dt);  lo.y = i8x2_to_f16x2(v[t].x, 16, dt);
-        lo.z = i8x2_to_f16x2(v[t].y, 0, dt);  lo.w = i8x2_to_f16x2(v[t].y, 16, dt);
-        hi.x = i8x2_to_f16x2(v[t].z, 0, dt);  hi.y = i8x2_to_f16x2(v[t].z, 16, dt);
-        hi.z = i8x2_to_f16x2(v[t].w, 0, dt);  hi.w = i8x2_to_f16x2(v[t].w, 16, dt);
+        const uint32_t d2 = d[t] | (d[t] << 16);
+        i8x4_to_f16x4(v[t].x, d2, lo.x, lo.y);
+        i8x4_to_f16x4(v[t].y, d2, lo.z, lo.w);
+        i8x4_to_f16x4(v[t].z, d2, hi.x, hi.y);
+        i8x4_to_f16x4(v[t].w, d2, hi.z, hi.w);
         st_unit(base, key, u, lo);
         st_unit(base, key, u + 1, hi);
       }

@@ -65,6 +65,22 @@ MLA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Four int8 codes (one 32-bit word) times the fp16 scale d2 (both halves):
+// fp16(code x d) for each, as two fp16 pairs.  A biased byte c + 128 placed
+// under the fp16 exponent of 1024 reads as 1024 + c + 128, so subtracting
+// 1152 gives the code exactly; the product is then rounded once, the same
+// result as rounding the exact product code x d to fp16.
+MLA_DEVINL void i8x4_to_f16x4(uint32_t w, uint32_t d2, uint32_t& lo, uint32_t& hi) {
+  const uint32_t b = w ^ 0x80808080u;
+  const uint32_t h0 = __byte_perm(b, 0x64646464u, 0x4140), h1 = __byte_perm(b, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+  const __half2 d = *reinterpret_cast<const __half2*>(&d2);
+  const __half2 r0 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&h0), bias), d);
+  const __half2 r1 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&h1), bias), d);
+  lo = *reinterpret_cast<const uint32_t*>(&r0);
+  hi = *reinterpret_cast<const uint32_t*>(&r1);
+}
+
 MLA_DEVINL float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -214,18 +214,11 @@ __global__ void __launch_bounds__(256) cache_q8_0_to_f16_kernel(const int8_t* kv
     const int64_t row = u / (kRow / 16);
     const int c = static_cast<int>(u % (kRow / 16));
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(kv_q + row * kRow) + c);
-    const float d = __half2float(__ldg(kv_d + static_cast<int64_t>(c >> 1) * ld_d + row));
+    const uint32_t ds = __half_as_ushort(__ldg(kv_d + static_cast<int64_t>(c >> 1) * ld_d + row));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t h[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float a0 = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
-      const float a1 = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
-      const float a2 = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
-      const float a3 = static_cast<float>(static_cast<int8_t>(w[k] >> 24));
-      h[2 * k] = pack_f16x2(a0 * d, a1 * d);
-      h[2 * k + 1] = pack_f16x2(a2 * d, a3 * d);
-    }
+    for (int k = 0; k < 4; ++k) i8x4_to_f16x4(w[k], ds | (ds << 16), h[2 * k], h[2 * k + 1]);
     out[2 * u] = make_uint4(h[0], h[1], h[2], h[3]);
     out[2 * u + 1] = make_uint4(h[4], h[5], h[6], h[7]);
   }
