@@ -750,24 +750,48 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       };
 
       // One loop body (a register copy per tile keeps the hot code small).
-      fetch(u0, own, false);
-      send(u0, own);
+      if constexpr (kDecode) {
+        // Decode: the first fetch in the loop too (step t = -1), so that
+        // fetch, send and process each have one call site: the decode kernel
+        // is instruction-fetch bound.
 #pragma unroll 1
-      for (int t = 0; t < n; ++t) {
-        const int u = u0 + t;
-        // Check both phases this tile needs first, so that their latencies
-        // overlap; a phase not yet complete is waited for where it is needed.
-        const bool s_test = mbar_test(&B.s_full[(u + 1) & 1], ((u + 1) >> 1) & 1);
-        const bool x_test = tc::mbar_test_cluster(&B.x_full[u & 1], (u >> 1) & 1);
-        const bool s_ready = __all_sync(0xffffffffu, s_test) && t + 1 < n;
-        const bool x_ready = __all_sync(0xffffffffu, x_test);
-        if (t + 1 < n) {
-          fetch(u + 1, nxt, s_ready);
-          send(u + 1, nxt);
-        }
-        process(t, own, x_ready);
+        for (int t = -1; t < n; ++t) {
+          const int u = u0 + t;
+          bool s_ready = false, x_ready = false;
+          if (t >= 0) {
+            const bool s_test = mbar_test(&B.s_full[(u + 1) & 1], ((u + 1) >> 1) & 1);
+            const bool x_test = tc::mbar_test_cluster(&B.x_full[u & 1], (u >> 1) & 1);
+            s_ready = __all_sync(0xffffffffu, s_test) && t + 1 < n;
+            x_ready = __all_sync(0xffffffffu, x_test);
+          }
+          if (t + 1 < n) {
+            fetch(u + 1, nxt, s_ready);
+            send(u + 1, nxt);
+          }
+          if (t >= 0) process(t, own, x_ready);
 #pragma unroll
-        for (int e = 0; e < kKpt / 2; ++e) own[e] = nxt[e];
+          for (int e = 0; e < kKpt / 2; ++e) own[e] = nxt[e];
+        }
+      } else {
+        fetch(u0, own, false);
+        send(u0, own);
+#pragma unroll 1
+        for (int t = 0; t < n; ++t) {
+          const int u = u0 + t;
+          // Check both phases this tile needs first, so that their latencies
+          // overlap; a phase not yet complete is waited for where it is needed.
+          const bool s_test = mbar_test(&B.s_full[(u + 1) & 1], ((u + 1) >> 1) & 1);
+          const bool x_test = tc::mbar_test_cluster(&B.x_full[u & 1], (u >> 1) & 1);
+          const bool s_ready = __all_sync(0xffffffffu, s_test) && t + 1 < n;
+          const bool x_ready = __all_sync(0xffffffffu, x_test);
+          if (t + 1 < n) {
+            fetch(u + 1, nxt, s_ready);
+            send(u + 1, nxt);
+          }
+          process(t, own, x_ready);
+#pragma unroll
+          for (int e = 0; e < kKpt / 2; ++e) own[e] = nxt[e];
+        }
       }
       // ---- end of item -----------------------------------------------------------
       if constexpr (kEpi) {
@@ -1020,24 +1044,29 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       const int ct = 64 + q4 * 32 + lane;
       TileCursor<kDecode> cur;
       cur.init(a, first, stride);
+      // One pass past the last tile writes the last item's output (one call
+      // site of the epilogue: the decode kernel is instruction-fetch bound).
 #pragma unroll 1
-      for (int u = 0; ok && cur.valid(); ++u, cur.next()) {
-        const bool first_tile = cur.t == 0;
+      for (int u = 0; ok; ++u, cur.next()) {
+        const bool has = cur.valid();
+        const bool first_tile = has && cur.t == 0;
         if (first_tile) q_load(cur.it, k, cur.iter);
-        const int ls = u % kLatStages;
-        ok = ok && wait_all(&B.lat_tma[ls], (u / kLatStages) & 1, a);
-        if (!ok) break;
-        convert_share(sLat + ls * kLatStage, ct);
-        tc::fence_proxy_async();
-        mbar_arrive(&B.lat_full[ls]);
-        if (first_tile) {
+        if (has) {
+          const int ls = u % kLatStages;
+          ok = ok && wait_all(&B.lat_tma[ls], (u / kLatStages) & 1, a);
+          if (!ok) break;
+          convert_share(sLat + ls * kLatStage, ct);
+          tc::fence_proxy_async();
+          mbar_arrive(&B.lat_full[ls]);
+        }
+        if (first_tile || !has) {
           if (k > 0) epilogue(prev, k - 1);
+          if (!has) break;
           prev = cur.it;
           ++k;
         }
       }
     }
-    if (ok && k > 0) epilogue(prev, k - 1);
     }
   } else if (warp < kMmaWarp) {
     // ============================ loader =======================================
@@ -1194,10 +1223,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         const int n = it.n_tiles;
         ok = wait_all(&B.q_ready, k & 1, a);
         tc::fence_after_sync();
-        for (int t = 0; ok && t < 3 && t < n; ++t) ok = issue_qk(u + t);
-        if (ok && kEpi && n <= 3) tc::mma_commit_warp(&B.q_free);
-        for (int t = 0; ok && t < n; ++t) {
-          ok = issue_pv(u + t, t == 0, k);
+        // Step t: P.V of tile t (t >= 0), then the scores of tile t + 3.  One
+        // call site of each (the decode kernel is instruction-fetch bound).
+#pragma unroll 1
+        for (int t = -3; ok && t < n; ++t) {
+          if (t >= 0) ok = issue_pv(u + t, t == 0, k);
           if (ok && t + 3 < n) {
             ok = issue_qk(u + t + 3);
             if (ok && kEpi && t + 3 == n - 1) tc::mma_commit_warp(&B.q_free);
