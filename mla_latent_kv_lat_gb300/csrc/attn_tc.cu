@@ -847,7 +847,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       u0 += n;
       ++k;
     }
-  } else if (kEpi && warp < kLoaderWarp) {
+  } else if (kEpi && (warp < kLoaderWarp || (kDecode && !kQ8 && warp > kLoaderWarp && warp < kMmaWarp))) {
     if constexpr (!kDecode) {
     // ======================= Q loading and epilogue (prefill) ==================
     // Warp 8+q serves TMEM lane quadrant q: thread = query row i, the whole
@@ -952,6 +952,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     // these warps convert their share of every tile to fp16 (see
     // convert_share): in decode they have little else to do.  (A separate
     // copy of the prefill code: sharing it cost the prefill kernel ~10%.)
+    // The two converter warps after the loader warp run the same loop without
+    // the Q and output steps (one copy of the hot code: the decode kernel is
+    // instruction-fetch bound).
+    const bool epi = warp < kLoaderWarp;
     const int q4 = warp & 3;
     const int i = q4 * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
@@ -1038,10 +1042,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     Item prev;
     int k = 0;
     {
-      // Conversion share 64 + 32 q4 + lane; at an item's first tile, its Q
-      // first, then the tile, then the previous item's epilogue (its P.V has
-      // to finish anyway before the new item's first P.V may start).
-      const int ct = 64 + q4 * 32 + lane;
+      // Conversion share 64 + 32 q4 + lane (epilogue warps) or 32 (w - 1) +
+      // lane (converter warp w after the loader warp); at an item's first
+      // tile, its Q first, then the tile, then the previous item's epilogue
+      // (its P.V has to finish anyway before the new item's first P.V may
+      // start).
+      const int ct = epi ? 64 + q4 * 32 + lane : (warp - kLoaderWarp - 1) * 32 + lane;
       TileCursor<kDecode> cur;
       cur.init(a, first, stride);
       // One pass past the last tile writes the last item's output (one call
@@ -1049,7 +1055,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 #pragma unroll 1
       for (int u = 0; ok; ++u, cur.next()) {
         const bool has = cur.valid();
-        const bool first_tile = has && cur.t == 0;
+        const bool first_tile = epi && has && cur.t == 0;
         if (first_tile) q_load(cur.it, k, cur.iter);
         if (has) {
           const int ls = u % kLatStages;
@@ -1059,6 +1065,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
           tc::fence_proxy_async();
           mbar_arrive(&B.lat_full[ls]);
         }
+        if (!epi && !has) break;
         if (first_tile || !has) {
           if (k > 0) epilogue(prev, k - 1);
           if (!has) break;
@@ -1112,21 +1119,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
             tc::tma_load_3d(sRope + rs * kChunk, &tm_cache, &B.rope_full[rs], kLatent, key, 0);
           }
         }
-      } else if (kDecode && pt >= 32) {
-        // bf16 decode: two warps convert each landed latent tile to fp16 in
-        // place (exact over fp16's normal range).  A 16-byte unit holds 8
-        // consecutive values of one key, so the swizzle does not matter.
-        const int ct = pt - 32;                 // 0..63; the epilogue warps are 64..191
-        TileCursor<kDecode> cur;
-        cur.init(a, first, stride);
-        for (int u = 0; cur.valid(); ++u, cur.next()) {
-          const int ls = u % kLatStages;
-          if (!wait_all(&B.lat_tma[ls], (u / kLatStages) & 1, a)) break;
-          convert_share(sLat + ls * kLatStage, ct);
-          tc::fence_proxy_async();
-          mbar_arrive(&B.lat_full[ls]);
-        }
       }
+      // (bf16 decode: the two converter warps after this one run the
+      // epilogue warps' conversion loop.)
     } else {
       if (rank == 0)
         run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, first, stride);
