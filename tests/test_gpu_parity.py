@@ -166,7 +166,13 @@ def test_decode_chain_v3_b32_every_sequence():
     assert_tol(got[[0, -1]][:, heads], ref_u, TOL_BF16, "decode o (un-absorbed heads)")
 
 
-@pytest.mark.parametrize("lengths", [[1], [1, 2, 3], [2049, 4096, 17, 6000], [5000] * 3])
+# Many short sequences (more than there are clusters): every cluster runs
+# several pieces back to back, so the per-piece barrier phases (Q hand-over,
+# output hand-over, row sums) turn over many times within one launch.
+MANY_SHORT = [1 + (37 * i) % 300 for i in range(100)]
+
+
+@pytest.mark.parametrize("lengths", [[1], [1, 2, 3], [2049, 4096, 17, 6000], [5000] * 3, MANY_SHORT])
 def test_decode_chain_ragged_lengths(lengths):
     x = W.make_inputs("v3_decode_b32", n_head=32, lengths=lengths)
     bufs = run_decode(Dev(x))
@@ -240,8 +246,9 @@ def test_decode_chain_q8_b8_every_sequence():
     assert_tol(got[[0, -1]][:, heads], ref_u, TOL_Q8, "q8 decode o (un-absorbed heads)")
 
 
-def test_decode_q8_small_ragged():
-    x = W.make_inputs("v3_q8_decode_b8", n_head=16, lengths=[1, 33, 2050])
+@pytest.mark.parametrize("lengths", [[1, 33, 2050], MANY_SHORT])
+def test_decode_q8_small_ragged(lengths):
+    x = W.make_inputs("v3_q8_decode_b8", n_head=16, lengths=lengths)
     q8, c_kv, k_pe = _q8(x)
     bufs = run_decode(Dev(x, q8), q8=True)
     ref, _, _ = _decode_refs(x, c_kv, k_pe)
