@@ -20,7 +20,13 @@ Sources (web pages, cited by title and section):
   (czykbl.com/news/94940): sec. 2.1 (kv_lora_rank 512, key_length 576,
   value_length 512, nope 128, v 128, rope 64), sec. 3.2 (wk_b / wv_b layouts).
 * [KVRM] "ik_llama.cpp discussion #586 slow KV cache rm" (trdm.cn/news/546512):
-  the log line giving the q8_0 latent cache size at n_ctx 98304.
+  the log line giving the q8_0 latent cache size at n_ctx 98304, and the
+  context log of the same run (sec. "混合卸载配置解读": freq_base 10000.0,
+  freq_scale 0.025).
+* [KVC] "llama.cpp KV Cache 与注意力机制：环形缓冲到 Flash Attention"
+  (borninfreedom.github.io/posts/2026/07/blog-post-4): sec. 2.2 (new tokens
+  are written into cache slots found for them), sec. 2.3 (keys are rotated
+  by ``ggml_rope_ext`` with n_rot dimensions).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, brute force on tiny inputs, invariants, the pages' printed
@@ -212,6 +218,41 @@ def quantize_q8_0(x: np.ndarray):
     r = np.where(d[:, :, None] > 0, r, 0)
     codes = r.astype(np.int8).reshape(n, width)
     return codes, d.astype(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# The step before the path: new tokens' rows into the latent cache
+# ([MLA] sec. 3: the RoPE part is rotated by position and kept apart from the
+# latent part; [KVC] sec. 2.2-2.3; [KVRM] freq_base / freq_scale)
+# ---------------------------------------------------------------------------
+def rope_rotate(x: np.ndarray, pos, freq_base: float, freq_scale: float) -> np.ndarray:
+    """Rotary position encoding of the last dimension (d = 64 for k_pe).
+
+    Readings (the pages name ``ggml_rope_ext`` with n_rot = 64, freq_base and
+    freq_scale, but not the pairing or any extension of the frequencies):
+    dimensions (2i, 2i+1) form pair i (ggml's default, "normal" mode) and are
+    rotated by the angle theta_i = pos * freq_scale * freq_base^(-2i/d):
+    (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).  No other scaling.
+    ``pos`` broadcasts against x's leading dimensions.  float64.
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    assert d % 2 == 0
+    i = np.arange(d // 2, dtype=np.float64)
+    theta = _f64(pos)[..., None] * float(freq_scale) * np.power(float(freq_base), -2.0 * i / d)
+    c, s = np.cos(theta), np.sin(theta)
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+def cache_rows(c_kv_new: np.ndarray, k_pe_new: np.ndarray, pos, freq_base: float, freq_scale: float) -> np.ndarray:
+    """The cache rows of new tokens: [c_kv (512, as given) | RoPE(k_pe, pos) (64)],
+    float64 (the cache stores them in its element type: bf16, or q8_0 via
+    ``quantize_q8_0``)."""
+    return np.concatenate([_f64(c_kv_new), rope_rotate(k_pe_new, pos, freq_base, freq_scale)], axis=-1)
 
 
 def dequantize_q8_0(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:

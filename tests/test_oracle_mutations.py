@@ -65,3 +65,37 @@ def test_truncating_q8_0_quantiser_is_caught(monkeypatch):
     blk[0], blk[1] = 31.75, 0.625                     # 0.625 / 0.25 = 2.5
     codes, _ = O.quantize_q8_0(blk[None])
     assert codes[0, 1] != 3
+
+
+@pytest.mark.parametrize("which", ["sign", "split_half_pairs", "exponent_i_over_d"])
+def test_rope_mistakes_are_caught(monkeypatch, which):
+    """A wrong rotation sign, the split-half pairing or a frequency exponent
+    i/d instead of 2i/d, planted in a copy of the oracle's RoPE, fails the
+    RoPE pins."""
+    import tests.test_oracle_pins as P
+
+    def bad(x, pos, b, s):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        i = np.arange(d // 2, dtype=np.float64)
+        e = (i / d) if which == "exponent_i_over_d" else (2.0 * i / d)
+        th = np.asarray(pos, np.float64)[..., None] * s * np.power(b, -e)
+        c, sn = np.cos(th), np.sin(th)
+        if which == "sign":
+            sn = -sn
+        if which == "split_half_pairs":
+            x0, x1 = x[..., : d // 2], x[..., d // 2:]
+            return np.concatenate([x0 * c - x1 * sn, x0 * sn + x1 * c], axis=-1)
+        out = np.empty_like(x)
+        out[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * sn
+        out[..., 1::2] = x[..., 0::2] * sn + x[..., 1::2] * c
+        return out
+
+    monkeypatch.setattr(O, "rope_rotate", bad)
+    failed = 0
+    for pin in (P.test_rope_quarter_turn_of_pair_zero_closed_form, P.test_rope_frequency_of_each_pair_closed_form):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1

@@ -281,3 +281,68 @@ def test_q8_0_error_bound_and_code_range():
     d32 = (np.abs(x.reshape(64, 18, 32)).max(axis=2) / np.float32(127)).astype(np.float64)
     bound = d32 / 2 + 127 * np.abs(d.astype(np.float64) - d32) + 1e-12
     assert np.all(np.abs(deq - x.reshape(64, 18, 32)).max(axis=2) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# RoPE and the cache rows of new tokens ("llama.cpp KV Cache 与注意力机制"
+# sec. 2.3; freq_base / freq_scale from the context log of "ik_llama.cpp
+# discussion #586 slow KV cache rm")
+# ---------------------------------------------------------------------------
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(5).standard_normal((7, 64))
+    assert np.array_equal(O.rope_rotate(x, np.zeros(7), 10000.0, 0.025), x)
+
+
+def test_rope_quarter_turn_of_pair_zero_closed_form():
+    # pair 0 turns by pos * freq_scale (freq_base^0 = 1): at a quarter turn,
+    # e_0 -> e_1 and e_1 -> -e_0, every other dimension untouched (pairing
+    # (2i, 2i+1): a split-half pairing would move e_0 to e_32).
+    pos = (math.pi / 2) / 0.025
+    e0, e1 = np.zeros(64), np.zeros(64)
+    e0[0], e1[1] = 1.0, 1.0
+    r0 = O.rope_rotate(e0, pos, 10000.0, 0.025)
+    r1 = O.rope_rotate(e1, pos, 10000.0, 0.025)
+    assert abs(r0[1] - 1.0) < 1e-12 and np.abs(np.delete(r0, 1)).max() < 1e-12
+    assert abs(r1[0] + 1.0) < 1e-12 and np.abs(np.delete(r1, 0)).max() < 1e-12
+
+
+def test_rope_frequency_of_each_pair_closed_form():
+    # pair i turns by pos * s * b^(-2i/64): read the angle back from e_(2i).
+    b, s, pos = 10000.0, 0.025, 12345.0
+    for i in range(32):
+        e = np.zeros(64)
+        e[2 * i] = 1.0
+        r = O.rope_rotate(e, pos, b, s)
+        theta = pos * s * b ** (-2.0 * i / 64)
+        assert abs(r[2 * i] - math.cos(theta)) < 1e-9 and abs(r[2 * i + 1] - math.sin(theta)) < 1e-9
+
+
+def test_rope_preserves_pair_norms_and_scale_acts_on_position():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((5, 64))
+    pos = rng.integers(0, 100000, 5).astype(np.float64)
+    r = O.rope_rotate(x, pos, 10000.0, 0.025)
+    n = lambda v: v[:, 0::2] ** 2 + v[:, 1::2] ** 2
+    assert np.abs(n(r) - n(x)).max() < 1e-9
+    assert np.abs(r - O.rope_rotate(x, pos * 0.025, 10000.0, 1.0)).max() < 1e-9
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    # <R(m) q, R(n) k> = <R(m - n) q, k>: the property RoPE exists for.
+    rng = np.random.default_rng(7)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    for m, n in [(10, 3), (5000, 4990), (98303, 17)]:
+        lhs = O.rope_rotate(q, m, 10000.0, 0.025) @ O.rope_rotate(k, n, 10000.0, 0.025)
+        rhs = O.rope_rotate(q, m - n, 10000.0, 0.025) @ k
+        assert abs(lhs - rhs) < 1e-9 * (1 + abs(rhs))
+
+
+def test_cache_rows_keep_the_latent_part_and_rotate_the_rope_part():
+    rng = np.random.default_rng(8)
+    c, kp = rng.standard_normal((3, 512)), rng.standard_normal((3, 64))
+    pos = np.array([0, 7, 90000])
+    rows = O.cache_rows(c, kp, pos, 10000.0, 0.025)
+    assert rows.shape == (3, 576)
+    assert np.array_equal(rows[:, :512], c)
+    assert np.array_equal(rows[0, 512:], kp[0])
+    assert np.array_equal(rows[1:, 512:], O.rope_rotate(kp[1:], pos[1:], 10000.0, 0.025))
