@@ -206,9 +206,37 @@ int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_
 int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n,
                       int64_t ld_d, void* stream);
 
+/* The step before the path: write the cache rows of n new tokens (pages:
+ * "MLA matrix absorption in ik_llama.cpp" sec. 3 -- the RoPE part of a key is
+ * rotated by position and kept apart from the latent part; "llama.cpp KV
+ * Cache 与注意力机制" sec. 2.2-2.3 -- new tokens go to the cache slots found
+ * for them, keys rotated by ggml_rope_ext over n_rot = 64 dims; freq_base and
+ * freq_scale as in the context log of "ik_llama.cpp discussion #586").
+ * Row slot[j] of the cache receives [c_kv[j] (512, as given) | RoPE(k_pe[j],
+ * pos[j]) (64)], RoPE pairing dims (2i, 2i+1) and turning pair i by
+ * pos * freq_scale * freq_base^(-2i/64).
+ * c_kv  device bf16 [n][512]; k_pe device bf16 [n][64] (not yet rotated);
+ * pos   device int32 [n] positions (>= 0); slot device int64 [n] cache rows.
+ * kv    device bf16 [n_rows][576] cache, or NULL; kv_q / kv_d the q8_0 cache
+ *       (int8 [n_rows][576], fp16 [18][ld_d], ld_d >= n_rows) or both NULL;
+ *       at least one cache.  The q8_0 row is the quantisation (as
+ *       mla_quantize_q8_0) of the bf16 row.
+ * A slot outside [0, n_rows) or a negative position is skipped on the
+ * device and recorded as MLA_ERR_INVALID_ARG in the device error word.
+ * The angles use freq_base and freq_scale as the floats given (the type ggml
+ * keeps them in), computed and reduced to [-pi, pi] in fp64; sine, cosine and
+ * the rotation in fp32; one rounding to bf16.
+ * Host errors: n < 1, freq_base <= 1 or freq_scale <= 0 (MLA_ERR_INVALID_ARG),
+ * pointers as above (MLA_ERR_MISALIGNED for kv_d only when odd).             */
+int mla_rope_append(const void* c_kv, const void* k_pe, const int32_t* pos, const int64_t* slot,
+                    int32_t n, float freq_base, float freq_scale, void* kv, int8_t* kv_q,
+                    uint16_t* kv_d, int64_t ld_d, int64_t n_rows, void* stream);
+
 /* Synchronise `stream`, then return and clear the current device's error
- * word: MLA_OK, or the first device-side error (MLA_ERR_TIMEOUT) recorded
- * since the last call.  MLA_ERR_CUDA if the synchronisation itself fails.     */
+ * word: MLA_OK, or the first device-side error (MLA_ERR_TIMEOUT from a
+ * bounded wait, MLA_ERR_INVALID_ARG from mla_rope_append's slot check)
+ * recorded since the last call.  MLA_ERR_CUDA if the synchronisation itself
+ * fails.                                                                      */
 int mla_get_device_error(void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an

@@ -8,6 +8,7 @@ from .binding import (MLAError, declared_symbols, library_path, load_library, ma
                       mla_absorb_q, mla_attn_decode, mla_attn_decode_q8_0, mla_attn_decode_static,
                       mla_attn_prefill,
                       mla_attn_prefill_q8_0, mla_decode_workspace_size, mla_prefill_workspace_size, mla_get_device_error,
-                      mla_late_decompress, mla_quantize_q8_0, mla_selftest_wait_timeout, mla_status_string,
+                      mla_late_decompress, mla_quantize_q8_0, mla_rope_append, mla_selftest_wait_timeout,
+                      mla_status_string,
                       mla_version)
 from .pipeline import mla_decode, mla_prefill  # noqa: F401

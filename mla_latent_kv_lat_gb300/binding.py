@@ -56,6 +56,8 @@ _SIGS = {
     "mla_attn_decode_static": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P], ctypes.c_int),
     "mla_late_decompress": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
     "mla_quantize_q8_0": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "mla_rope_append": ([_P, _P, _P, _P, _I32, ctypes.c_float, ctypes.c_float, _P, _P, _P, _I64, _I64, _P],
+                        ctypes.c_int),
     "mla_get_device_error": ([_P], ctypes.c_int),
     "mla_selftest_wait_timeout": ([_I32, _P], ctypes.c_int),
     "mla_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -223,6 +225,28 @@ def mla_quantize_q8_0(kv, kv_q, kv_d, stream=None):
         _need(kv, "kv", torch.bfloat16, (n, ROW)), _need(kv_q, "kv_q", torch.int8, (n, ROW)),
         _need(kv_d, "kv_d", torch.float16), n, kv_d.shape[1], _stream(stream))
     _check("mla_quantize_q8_0", st)
+
+
+def mla_rope_append(c_kv, k_pe, pos, slot, kv=None, kv_q=None, kv_d=None, freq_base: float = 10000.0,
+                    freq_scale: float = 0.025, stream=None):
+    """New tokens' rows into the cache(s): row slot[j] <- [c_kv[j] | RoPE(k_pe[j], pos[j])]."""
+    n = c_kv.shape[0]
+    if kv is None and kv_q is None:
+        raise ValueError("mla_rope_append needs a bf16 cache (kv), a q8_0 cache (kv_q, kv_d) or both")
+    n_rows = kv.shape[0] if kv is not None else kv_q.shape[0]
+    kvp = _need(kv, "kv", torch.bfloat16, (n_rows, ROW)) if kv is not None else None
+    if kv_q is not None:
+        if kv_d is None or kv_d.dim() != 2 or kv_d.shape[0] != Q8_BLOCKS:
+            raise ValueError(f"kv_d must have shape ({Q8_BLOCKS}, ld_d)")
+        kqp = _need(kv_q, "kv_q", torch.int8, (n_rows, ROW))
+        kdp, ld_d = _need(kv_d, "kv_d", torch.float16), kv_d.shape[1]
+    else:
+        kqp, kdp, ld_d = None, None, 0
+    st = load_library().mla_rope_append(
+        _need(c_kv, "c_kv", torch.bfloat16, (n, KV_LORA_RANK)), _need(k_pe, "k_pe", torch.bfloat16, (n, QK_ROPE)),
+        _need(pos, "pos", torch.int32, (n,)), _need(slot, "slot", torch.int64, (n,)), n, float(freq_base),
+        float(freq_scale), kvp, kqp, kdp, ld_d, n_rows, _stream(stream))
+    _check("mla_rope_append", st)
 
 
 def mla_get_device_error(stream=None) -> int:

@@ -3,6 +3,9 @@
 // in the kernels launched from here; there is no host or fallback compute.
 #include <stdint.h>
 
+#include <math.h>
+
+#include "append.cuh"
 #include "kernels.cuh"
 
 namespace mla {
@@ -231,6 +234,39 @@ int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, i
   if (n < 1 || ld_d < n) return MLA_ERR_INVALID_ARG;
   if ((n * kQ8Blocks + 7) / 8 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   return to_status(launch_quantize_q8_0(kv, kv_q, kv_d, n, ld_d, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_rope_append(const void* c_kv, const void* k_pe, const int32_t* pos, const int64_t* slot, int32_t n,
+                    float freq_base, float freq_scale, void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t ld_d,
+                    int64_t n_rows, void* stream) {
+  int s = check_ptrs({c_kv, k_pe, pos, slot});
+  if (s != MLA_OK) return s;
+  if (n < 1 || n_rows < 1) return MLA_ERR_INVALID_ARG;
+  if (!(freq_base > 1.f) || !(freq_scale > 0.f) || !isfinite(freq_base) || !isfinite(freq_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (kv == nullptr && kv_q == nullptr) return MLA_ERR_INVALID_ARG;
+  if ((kv_q == nullptr) != (kv_d == nullptr)) return MLA_ERR_INVALID_ARG;
+  if (kv != nullptr && !aligned16(kv)) return MLA_ERR_MISALIGNED;
+  if (kv_q != nullptr) {
+    if (!aligned16(kv_q)) return MLA_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(kv_d) & 1u) return MLA_ERR_MISALIGNED;
+    if (ld_d < n_rows) return MLA_ERR_INVALID_ARG;
+  }
+  RopeAppendArgs a = {};
+  a.c_kv = static_cast<const uint16_t*>(c_kv);
+  a.k_pe = static_cast<const uint16_t*>(k_pe);
+  a.pos = pos;
+  a.slot = slot;
+  a.n = n;
+  a.kv = static_cast<uint16_t*>(kv);
+  a.kv_q = kv_q;
+  a.kv_d = kv_d;
+  a.ld_d = ld_d;
+  a.n_rows = n_rows;
+  if (error_word(&a.err) != cudaSuccess) return MLA_ERR_CUDA;
+  for (int i = 0; i < kRope / 2; ++i)
+    a.freq[i] = static_cast<double>(freq_scale) * pow(static_cast<double>(freq_base), -2.0 * i / kRope);
+  return to_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
 }
 
 int mla_get_device_error(void* stream) {

@@ -1,0 +1,101 @@
+// The step before the attention path: the rows of new tokens into the latent
+// cache, bf16 and/or q8_0 (pages: "MLA matrix absorption in ik_llama.cpp"
+// sec. 3 -- the RoPE part of a key is rotated by position, the latent part is
+// not; "llama.cpp KV Cache 与注意力机制" sec. 2.2-2.3 -- slots and
+// ggml_rope_ext over n_rot = 64 dims).  HBM-bound: 1164 bytes in and up to
+// 1764 bytes out per token.
+#include "append.cuh"
+#include "kernels.cuh"
+
+namespace mla {
+namespace {
+
+constexpr double kTwoPi = 6.283185307179586;
+
+// Rotate this lane's 8 RoPE values (pairs 4 lane .. 4 lane + 3; dims (2i, 2i+1)
+// form pair i) by pos * freq[i].  The angle and its reduction to [-pi, pi] in
+// fp64 (exact enough for positions far beyond any cache), sine and cosine of
+// the reduced angle and the rotation in fp32, rounded once to bf16.
+MLA_DEVINL uint4 rope8(uint4 v, int32_t pos, const double* freq, int lane) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const double th = static_cast<double>(pos) * freq[4 * lane + q];
+    const double r = fma(-rint(th * (1.0 / kTwoPi)), kTwoPi, th);
+    float sn, cs;
+    sincosf(static_cast<float>(r), &sn, &cs);
+    const float2 x = bf16x2_to_f32(w[q]);
+    w[q] = pack_bf16x2(x.x * cs - x.y * sn, x.x * sn + x.y * cs);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One warp per new token, three passes over the 576-value row: latent values
+// [0, 256), [256, 512), then the RoPE values (lanes 0..7).  A lane holds 8
+// consecutive values (16 bytes); four lanes make one q8_0 block, quantised by
+// the rules of mla_quantize_q8_0.
+__global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); j < a.n; j += stride) {
+    const int64_t s = a.slot[j];
+    const int32_t p = a.pos[j];
+    if (s < 0 || s >= a.n_rows || p < 0) {
+      if (lane == 0) record_error(a.err, MLA_ERR_INVALID_ARG);
+      continue;
+    }
+#pragma unroll 1
+    for (int h = 0; h < 3; ++h) {
+      const bool active = h < 2 || lane < 8;
+      const int col = h < 2 ? 256 * h + 8 * lane : kLatent + 8 * lane;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (active) {
+        if (h < 2) {
+          v = __ldg(reinterpret_cast<const uint4*>(a.c_kv + j * kLatent + col));
+        } else {
+          v = rope8(__ldg(reinterpret_cast<const uint4*>(a.k_pe + j * kRope + 8 * lane)), p, a.freq, lane);
+        }
+        if (a.kv != nullptr) *reinterpret_cast<uint4*>(a.kv + s * kRow + col) = v;
+      }
+      if (a.kv_q != nullptr) {
+        float x[8];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = bf16x2_to_f32(w[q]);
+          x[2 * q] = f.x;
+          x[2 * q + 1] = f.y;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const float d = amax / 127.0f;
+        uint32_t c[2] = {0u, 0u};
+        if (amax > 0.f) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int q = max(-127, min(127, static_cast<int>(roundf(x[e] / d))));
+            c[e >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (e & 3));
+          }
+        }
+        if (active) {
+          *reinterpret_cast<uint2*>(a.kv_q + s * kRow + col) = make_uint2(c[0], c[1]);
+          if ((lane & 3) == 0) a.kv_d[static_cast<int64_t>(col / kQ8Block) * a.ld_d + s] = __half_as_ushort(__float2half_rn(d));
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream) {
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  const unsigned blocks = static_cast<unsigned>(max(static_cast<int64_t>(1), min(cap, (a.n + 7) / 8)));
+  rope_append_kernel<<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

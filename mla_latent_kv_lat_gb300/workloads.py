@@ -214,3 +214,31 @@ def sample_rows(n: int, k: int, seed: int = 0, must: tuple = ()) -> np.ndarray:
         if int(r) not in base:
             out.append(int(r))
     return np.array(sorted(out), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# New tokens for the cache-append step (mla_rope_append)
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class AppendInputs:
+    c_kv: np.ndarray      # [n, 512] bf16 values as float32
+    k_pe: np.ndarray      # [n, 64]  bf16 values as float32 (not yet rotated)
+    pos: np.ndarray       # [n] int32 positions
+    slot: np.ndarray      # [n] int64 distinct cache rows in [0, n_rows)
+    n_rows: int
+
+
+def make_append_inputs(n: int, n_rows: int, seed: int = 0, max_pos: int = 98304) -> AppendInputs:
+    """n new tokens with N(0,1) bf16 latent and RoPE parts (the distributions
+    of the cache rows in every workload), positions uniform in [0, max_pos)
+    plus the two ends, and distinct slots drawn from the cache's n_rows rows."""
+    assert 1 <= n <= n_rows
+    rng = np.random.default_rng(seed)
+    c_kv = to_bf16(rng.standard_normal((n, KV_LORA_RANK), dtype=np.float32))[0]
+    k_pe = to_bf16(rng.standard_normal((n, QK_ROPE), dtype=np.float32))[0]
+    pos = rng.integers(0, max_pos, n).astype(np.int32)
+    pos[0] = 0
+    if n > 1:
+        pos[-1] = max_pos - 1
+    slot = rng.permutation(n_rows)[:n].astype(np.int64)
+    return AppendInputs(c_kv, k_pe, pos, slot, n_rows)

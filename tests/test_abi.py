@@ -74,6 +74,20 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, None, pw, GOOD, None, None) == -4
     assert lib.mla_attn_prefill(_dims(), GOOD, GOOD, GOOD, 10, 4, 0, ODD, pw, GOOD, None, None) == -3
     assert lib.mla_attn_prefill_q8_0(_dims(), GOOD, GOOD, GOOD, None, 10, 4, 0, GOOD, pw, GOOD, None, None) == -1
+    # cache append: sizes, frequencies, at least one cache, the q8_0 pair together, alignment
+    ra = lib.mla_rope_append
+    assert ra(GOOD, GOOD, GOOD, GOOD, 0, 10000.0, 0.025, GOOD, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, GOOD, None, None, 0, 0, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 1.0, 0.025, GOOD, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.0, GOOD, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, float("nan"), GOOD, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, None, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, None, GOOD, None, 8, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, None, GOOD, GOOD, 7, 8, None) == -1
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, None, GOOD, P(0x100001), 8, 8, None) == -3
+    assert ra(GOOD, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, ODD, None, None, 0, 8, None) == -3
+    assert ra(None, GOOD, GOOD, GOOD, 4, 10000.0, 0.025, GOOD, None, None, 0, 8, None) == -1
+    assert ra(GOOD, GOOD, ODD, GOOD, 4, 10000.0, 0.025, GOOD, None, None, 0, 8, None) == -3
     # decode: workspace size is checked on the host
     need = lib.mla_decode_workspace_size(_dims(128), 32, 32768)
     assert need > 0

@@ -296,3 +296,102 @@ def test_invalid_arguments_return_status():
                             torch.ones(1, dtype=torch.int32, device="cuda"), 8, ws, o_lat[:1])
     assert e.value.status == -4                      # workspace too small
     _check_no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# The step before the path: mla_rope_append writes new tokens' cache rows
+# ---------------------------------------------------------------------------
+# The entry point takes freq_base / freq_scale as float (as ggml keeps them):
+# the oracle turns by the same values (0.025 is not a float; its float is
+# 1.5e-8 larger, which moves angles near 2000 rad by 3e-5).
+FB, FS = float(np.float32(10000.0)), float(np.float32(0.025))
+
+
+def _append_dev(a: W.AppendInputs):
+    c = torch.from_numpy(W.to_bf16(a.c_kv)[1]).view(torch.bfloat16).cuda()
+    k = torch.from_numpy(W.to_bf16(a.k_pe)[1]).view(torch.bfloat16).cuda()
+    return c, k, torch.from_numpy(a.pos).cuda(), torch.from_numpy(a.slot).cuda()
+
+
+def _caches(n_rows, ld_d):
+    kv = torch.zeros(n_rows, 576, dtype=torch.bfloat16, device="cuda")
+    kv_q = torch.zeros(n_rows, 576, dtype=torch.int8, device="cuda")
+    kv_d = torch.zeros(18, ld_d, dtype=torch.float16, device="cuda")
+    return kv, kv_q, kv_d
+
+
+@pytest.mark.parametrize("n,n_rows", [(1, 4), (333, 1000), (4096, 98304)])
+def test_rope_append_matches_oracle(n, n_rows):
+    a = W.make_append_inputs(n, n_rows, seed=n)
+    c, k, pos, slot = _append_dev(a)
+    kv, kv_q, kv_d = _caches(n_rows, n_rows + 3)
+    mla.mla_rope_append(c, k, pos, slot, kv=kv, kv_q=kv_q, kv_d=kv_d, freq_base=FB, freq_scale=FS)
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    got = kv.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = W.to_bf16(O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS).astype(np.float32))[1]
+    rows = got[a.slot]
+    # The latent part is copied: bit-exact.  The RoPE part: the device rotates
+    # in fp32 (angle reduced in fp64) and rounds once to bf16, so it is within
+    # half a bf16 step (2^-8 relative) of the exact rotation, plus the fp32
+    # error of ~1e-6 of the pair's magnitude (which matters only where the
+    # two terms cancel).
+    assert np.array_equal(rows[:, :512], ref[:, :512])
+    exact = O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS)[:, 512:]
+    pair = np.repeat(np.maximum(np.abs(a.k_pe[:, 0::2]), np.abs(a.k_pe[:, 1::2])), 2, axis=1).astype(np.float64)
+    err = np.abs(W.bf16_bits_to_f32(rows[:, 512:]).astype(np.float64) - exact)
+    assert (err <= 2.0 ** -8 * np.abs(exact) + 1e-6 * pair).all()
+    assert (rows[:, 512:] != ref[:, 512:]).mean() < 1e-2
+    # rows not written stay untouched
+    untouched = np.setdiff1d(np.arange(n_rows), a.slot)
+    assert not got[untouched].any()
+    # the q8_0 rows: the oracle's quantisation of the device's own bf16 rows, bit-exact
+    codes, scales = O.quantize_q8_0(W.bf16_bits_to_f32(rows))
+    assert np.array_equal(kv_q.cpu().numpy()[a.slot], codes)
+    got_d = kv_d.cpu().numpy()
+    assert np.array_equal(got_d[:, a.slot].T.view(np.uint16), scales.view(np.uint16))
+    assert not got_d[:, n_rows:].view(np.uint16).any()
+    # one cache at a time writes the same rows
+    kv2, kq2, kd2 = _caches(n_rows, n_rows + 3)
+    mla.mla_rope_append(c, k, pos, slot, kv=kv2)
+    mla.mla_rope_append(c, k, pos, slot, kv_q=kq2, kv_d=kd2)
+    torch.cuda.synchronize()
+    assert torch.equal(kv2.view(torch.int16), kv.view(torch.int16))
+    assert torch.equal(kq2, kv_q) and torch.equal(kd2.view(torch.int16), kv_d.view(torch.int16))
+
+
+def test_rope_append_then_decode_reads_the_rows():
+    # a sequence whose rows were all written by mla_rope_append (positions
+    # 0..L-1, the RoPE part rotated by position) decodes as the oracle does
+    # on those rows
+    L, H = 700, 32
+    a = W.make_append_inputs(L, L, seed=11)
+    a.pos[:] = np.arange(L, dtype=np.int32)
+    a.slot[:] = np.arange(L, dtype=np.int64)
+    c, k, pos, slot = _append_dev(a)
+    kv, kv_q, kv_d = _caches(L, L)
+    mla.mla_rope_append(c, k, pos, slot, kv=kv, kv_q=kv_q, kv_d=kv_d)
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    x = W.make_inputs("v3_decode_b32", n_head=H, lengths=[L])
+    rows = W.bf16_bits_to_f32(kv.view(torch.int16).cpu().numpy().view(np.uint16))
+    x = W.Inputs(x.wl, rows[:, :512], rows[:, 512:], x.q_nope, x.q_pe, x.wk_b, x.wv_b, x.seq_len, x.seq_start)
+    d = Dev(x)
+    d.kv = kv                                   # decode reads the cache the append wrote
+    bufs = run_decode(d)
+    ref, _, _ = _decode_refs(x, x.c_kv, x.k_pe)
+    assert_tol(bufs.o.cpu().numpy(), ref, TOL_BF16, "decode o on appended rows")
+
+
+def test_rope_append_out_of_range_slot_is_skipped_and_reported():
+    a = W.make_append_inputs(8, 16, seed=3)
+    a.slot[3] = 16                              # one past the end
+    c, k, pos, slot = _append_dev(a)
+    kv, kv_q, kv_d = _caches(16, 16)
+    mla.mla_rope_append(c, k, pos, slot, kv=kv, kv_q=kv_q, kv_d=kv_d)
+    assert mla.mla_get_device_error() == -1     # MLA_ERR_INVALID_ARG, read and cleared
+    got = kv.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = W.to_bf16(O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS).astype(np.float32))[1]
+    ok = [j for j in range(8) if j != 3]
+    assert np.array_equal(got[a.slot[ok], :512], ref[ok, :512])
+    assert mla.mla_get_device_error() == 0
