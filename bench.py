@@ -55,6 +55,15 @@ def decode_bytes(wl: W.Workload, x: W.Inputs) -> float:
     return float(x.seq_len.astype(np.int64).sum()) * row + q + o
 
 
+# bytes per appended token: c_kv + k_pe in (bf16), position and slot, the bf16
+# row and the q8_0 row (codes + 18 fp16 scales) out
+APPEND_TOKEN_BYTES = (512 + 64) * 2 + 4 + 8 + 576 * 2 + 576 + 18 * 2
+
+
+def append_bytes(wl: W.Workload) -> float:
+    return float(wl.T) * APPEND_TOKEN_BYTES
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -140,10 +149,31 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def setup_append(wl, torch):
+    import mla_latent_kv_lat_gb300 as mla
+    a = W.make_append_inputs(wl.T, wl.n_kv)
+    d = {"c_kv": torch.from_numpy(W.to_bf16(a.c_kv)[1]).view(torch.bfloat16).cuda(),
+         "k_pe": torch.from_numpy(W.to_bf16(a.k_pe)[1]).view(torch.bfloat16).cuda(),
+         "pos": torch.from_numpy(a.pos).cuda(), "slot": torch.from_numpy(a.slot).cuda()}
+    caches = {"kv": torch.zeros(wl.n_kv, 576, dtype=torch.bfloat16, device="cuda"),
+              "kv_q": torch.zeros(wl.n_kv, 576, dtype=torch.int8, device="cuda"),
+              "kv_d": torch.zeros(18, wl.n_kv, dtype=torch.float16, device="cuda")}
+
+    def step(stream=None, ev=None):
+        if ev:
+            ev[0].record()
+        mla.mla_rope_append(d["c_kv"], d["k_pe"], d["pos"], d["slot"], stream=stream, **caches)
+        if ev:
+            ev[1].record()
+    return wl, a, d, caches, step, 1
+
+
 def setup_workload(name, torch):
     import mla_latent_kv_lat_gb300 as mla
     from mla_latent_kv_lat_gb300 import pipeline as P
     wl = W.WORKLOADS[name]
+    if wl.kind == "append":
+        return setup_append(wl, torch)
     x = W.make_inputs(wl)
 
     def dev(a):
@@ -255,14 +285,14 @@ def run_ours(args, torch, dist, rank, world):
         roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst"}
     else:
-        units = decode_bytes(wl, x)
+        units = append_bytes(wl) if wl.kind == "append" else decode_bytes(wl, x)
         value = units * world / (ms_step * 1e-3) / 1e9
         unit = "GB/s"
-        ach = decode_bytes(wl, x) / (attn_avg * 1e-3) / 1e9
+        ach = units / (attn_avg * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} HBM copy"}
-    kname = "attn_tc_kernel"
+    kname = "rope_append_kernel" if wl.kind == "append" else "attn_tc_kernel"
     roof["traffic"] = recorded_traffic(kname, wl.name)
     roof["kernel"] = kname
     roof["attn_ms"] = round(attn_avg, 4)
@@ -277,8 +307,12 @@ def run_ours(args, torch, dist, rank, world):
                       "l2": "flushed before every step (512 MB write)"},
            "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clk.summary(),
            "wall_s_timed": round(t_wall, 3)}
-    out["e2e"] = e2e_prefill(args, torch, wl, x, d, bufs) if wl.kind == "prefill" else e2e_decode(args, torch, wl, x, d,
-                                                                                                   bufs)
+    if wl.kind == "prefill":
+        out["e2e"] = e2e_prefill(args, torch, wl, x, d, bufs)
+    elif wl.kind == "append":
+        out["e2e"] = e2e_append(args, torch, wl, d, bufs)
+    else:
+        out["e2e"] = e2e_decode(args, torch, wl, x, d, bufs)
     if args.with_decode and wl.kind == "prefill":
         out["decode"] = secondary(args, torch, DECODE_WORKLOAD, flush, pk, pk_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -322,6 +356,38 @@ def e2e_prefill(args, torch, wl, x, d, bufs):
     ms = sum(ts) / len(ts)
     return {"value": round(attn_flops(wl, x) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def e2e_append(args, torch, wl, d, caches):
+    """The append through the public entry point with its inputs copied from
+    pinned host memory every step; the step's result is the cache rows in HBM
+    (read by the attention kernels there), so the host reads back only the
+    device status word that says they were all written."""
+    import mla_latent_kv_lat_gb300 as mla
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+    def one():
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        mla.mla_rope_append(d["c_kv"], d["k_pe"], d["pos"], d["slot"], **caches)
+        if mla.mla_get_device_error() != 0:
+            raise RuntimeError("device error during the append e2e run")
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    return {"value": round(append_bytes(wl) / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4}
 
 
 def e2e_decode(args, torch, wl, x, d, bufs):
@@ -369,11 +435,16 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_sample(wl: W.Workload, x: W.Inputs, rows: int):
+def oracle_sample(wl: W.Workload, x, rows: int):
     """Run the oracle (un-absorbed definition) on the first `rows` query rows
-    (prefill) or sequences (decode); returns (seconds, units done)."""
+    (prefill), sequences (decode) or new tokens (append); returns (seconds,
+    units done)."""
     from oracle import mla_oracle as O
     t0 = time.perf_counter()
+    if wl.kind == "append":
+        r = O.cache_rows(x.c_kv[:rows], x.k_pe[:rows], x.pos[:rows], 10000.0, 0.025)
+        O.quantize_q8_0(r.astype(np.float32))
+        return time.perf_counter() - t0, rows * APPEND_TOKEN_BYTES
     if wl.kind == "prefill":
         c_kv, k_pe = x.c_kv, x.k_pe
         if wl.cache == "q8_0":
@@ -395,24 +466,26 @@ def oracle_sample(wl: W.Workload, x: W.Inputs, rows: int):
 
 
 def cpu_baseline(wl, x, unit, budget_s=20.0):
-    rows = 4 if wl.kind == "prefill" else 1
+    rows = 4 if wl.kind != "decode" else 1
+    cap = wl.B if wl.kind == "decode" else wl.T
     sec, units = oracle_sample(wl, x, rows)
     # grow the sample toward the time budget, then report the largest
-    while sec < budget_s / 4 and rows < (wl.T if wl.kind == "prefill" else wl.B):
-        rows = min(rows * 4, wl.T if wl.kind == "prefill" else wl.B)
+    while sec < budget_s / 4 and rows < cap:
+        rows = min(rows * 4, cap)
         sec, units = oracle_sample(wl, x, rows)
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    what = f"last {rows} query rows (all heads)" if wl.kind == "prefill" else f"first {rows} sequences"
+    what = {"prefill": f"last {rows} query rows (all heads)", "decode": f"first {rows} sequences",
+            "append": f"first {rows} new tokens (rows + q8_0)"}[wl.kind]
     return {"value": units / sec / scale, "unit": unit, "cores": blas_threads(), "kind": "oracle",
             "sample": f"{what} of {wl.name}, un-absorbed numpy fp64 oracle, {sec:.2f} s"}
 
 
 def run_reference(args):
     wl = W.WORKLOADS[args.workload]
-    x = W.make_inputs(wl)
+    x = W.make_append_inputs(wl.T, wl.n_kv) if wl.kind == "append" else W.make_inputs(wl)
     unit = "TFLOP/s" if wl.kind == "prefill" else "GB/s"
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    rows = 32 if wl.kind == "prefill" else 1
+    rows = {"prefill": 32, "decode": 1, "append": 4096}[wl.kind]
     for _ in range(args.warmup):
         oracle_sample(wl, x, rows)
     tot_s = tot_u = 0.0
@@ -421,7 +494,8 @@ def run_reference(args):
         tot_s += s
         tot_u += u
     value = tot_u / tot_s / scale
-    what = f"last {rows} query rows" if wl.kind == "prefill" else f"first {rows} sequence"
+    what = {"prefill": f"last {rows} query rows", "decode": f"first {rows} sequence",
+            "append": f"first {rows} new tokens"}[wl.kind]
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",

@@ -264,8 +264,16 @@ int mla_rope_append(const void* c_kv, const void* k_pe, const int32_t* pos, cons
   a.ld_d = ld_d;
   a.n_rows = n_rows;
   if (error_word(&a.err) != cudaSuccess) return MLA_ERR_CUDA;
-  for (int i = 0; i < kRope / 2; ++i)
-    a.freq[i] = static_cast<double>(freq_scale) * pow(static_cast<double>(freq_base), -2.0 * i / kRope);
+  // turns per position of pair i, frac(t_i) as 0.64 fixed point: two exact
+  // 32-bit halves of the double's fraction
+  const double kTwoPi = 6.283185307179586;
+  for (int i = 0; i < kRope / 2; ++i) {
+    double t = static_cast<double>(freq_scale) * pow(static_cast<double>(freq_base), -2.0 * i / kRope) / kTwoPi;
+    t -= floor(t);
+    const double hi = floor(ldexp(t, 32));
+    const double lo = nearbyint(ldexp(ldexp(t, 32) - hi, 32));
+    a.turn[i] = (static_cast<uint64_t>(hi) << 32) + static_cast<uint64_t>(lo);
+  }
   return to_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -10,20 +10,19 @@
 namespace mla {
 namespace {
 
-constexpr double kTwoPi = 6.283185307179586;
-
 // Rotate this lane's 8 RoPE values (pairs 4 lane .. 4 lane + 3; dims (2i, 2i+1)
-// form pair i) by pos * freq[i].  The angle and its reduction to [-pi, pi] in
-// fp64 (exact enough for positions far beyond any cache), sine and cosine of
-// the reduced angle and the rotation in fp32, rounded once to bf16.
-MLA_DEVINL uint4 rope8(uint4 v, int32_t pos, const double* freq, int lane) {
+// form pair i) by pos * t_i turns.  The fraction of a turn is exact integer
+// arithmetic (the low 64 bits of pos * turn[i]); its top 32 bits give the
+// angle as a float in [0, 2) half-turns for sincospif (error < 2^-23 rad);
+// the rotation is in fp32, rounded once to bf16.
+MLA_DEVINL uint4 rope8(uint4 v, int32_t pos, const uint64_t* turn, int lane) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const double th = static_cast<double>(pos) * freq[4 * lane + q];
-    const double r = fma(-rint(th * (1.0 / kTwoPi)), kTwoPi, th);
+    const uint64_t f = static_cast<uint64_t>(static_cast<uint32_t>(pos)) * turn[4 * lane + q];
+    const float half_turns = static_cast<float>(static_cast<uint32_t>(f >> 32)) * 0x1p-31f;
     float sn, cs;
-    sincosf(static_cast<float>(r), &sn, &cs);
+    sincospif(half_turns, &sn, &cs);
     const float2 x = bf16x2_to_f32(w[q]);
     w[q] = pack_bf16x2(x.x * cs - x.y * sn, x.x * sn + x.y * cs);
   }
@@ -53,7 +52,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
         if (h < 2) {
           v = __ldg(reinterpret_cast<const uint4*>(a.c_kv + j * kLatent + col));
         } else {
-          v = rope8(__ldg(reinterpret_cast<const uint4*>(a.k_pe + j * kRope + 8 * lane)), p, a.freq, lane);
+          v = rope8(__ldg(reinterpret_cast<const uint4*>(a.k_pe + j * kRope + 8 * lane)), p, a.turn, lane);
         }
         if (a.kv != nullptr) *reinterpret_cast<uint4*>(a.kv + s * kRow + col) = v;
       }

@@ -16,7 +16,10 @@ struct RopeAppendArgs {
   int64_t ld_d;
   int64_t n_rows;
   int* err;
-  double freq[32];        // freq_scale * freq_base^(-2i/64): pair i turns by pos * freq[i]
+  // Pair i turns by pos * freq_scale * freq_base^(-2i/64) radians, i.e.
+  // pos * t_i full turns; turn[i] = frac(t_i) as a 0.64 fixed-point number,
+  // so that frac(pos * t_i) is the low 64 bits of the integer product.
+  uint64_t turn[32];
 };
 
 cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream);

@@ -66,7 +66,7 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 class Workload:
     """One named workload: a prefill chunk or a batch of decode queries."""
     name: str
-    kind: str                 # "prefill" | "decode"
+    kind: str                 # "prefill" | "decode" | "append" (new tokens into the cache)
     n_head: int
     cache: str                # "bf16" | "q8_0"
     T: int = 0                # prefill: query tokens
@@ -104,6 +104,13 @@ WORKLOADS = {
     "v3_q8_decode_b8": Workload(
         "v3_q8_decode_b8", "decode", 128, "q8_0", B=8, len_lo=98304, len_hi=98304,
         describe="DeepSeek-V3 shape, q8_0 latent cache, 8 sequences decoding at length 98304"),
+    # The step before the path: T new tokens' rows (RoPE applied) into a bf16
+    # and a q8_0 cache of n_kv rows, at distinct random slots -- the fill of
+    # the 98304-row q8_0 cache of the V3 q8_0 workloads.
+    "v3_cache_append_98304": Workload(
+        "v3_cache_append_98304", "append", 128, "bf16+q8_0", T=98304, n_kv=98304,
+        describe="cache append: 98304 new tokens' rows (RoPE on the 64-d part) into a bf16 and a "
+                 "q8_0 latent cache of 98304 rows at random slots"),
 }
 
 
