@@ -224,8 +224,9 @@ int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n,
  * A slot outside [0, n_rows) or a negative position is skipped on the
  * device and recorded as MLA_ERR_INVALID_ARG in the device error word.
  * The angles use freq_base and freq_scale as the floats given (the type ggml
- * keeps them in), computed and reduced to [-pi, pi] in fp64; sine, cosine and
- * the rotation in fp32; one rounding to bf16.
+ * keeps them in); the fraction of a turn is exact fixed-point arithmetic
+ * (error < 2^-23 rad at any position), sine, cosine and the rotation are
+ * fp32, with one rounding to bf16.
  * Host errors: n < 1, freq_base <= 1 or freq_scale <= 0 (MLA_ERR_INVALID_ARG),
  * pointers as above (MLA_ERR_MISALIGNED for kv_d only when odd).             */
 int mla_rope_append(const void* c_kv, const void* k_pe, const int32_t* pos, const int64_t* slot,
