@@ -34,7 +34,9 @@ METRIC = "MLA attn TFLOP/s (prefill) & HBM GB/s (decode) on 1 GB300, % of roofli
 DEFAULT_WORKLOAD = "lite_t4096"
 DECODE_WORKLOAD = "v3_decode_b32"
 FLOP_PER_PAIR_HEAD = 2 * 576 + 2 * 512          # scores (576-d) + latent weighted sum (512-d)
-KERNEL_SOURCES = ["attn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"]
+# sources whose hash dates the ncu traffic recorded for each kernel
+KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"],
+                  "rope_append_kernel": ["append.cu", "append.cuh", "common.cuh"]}
 
 
 # ---------------------------------------------------------------------------
@@ -71,9 +73,9 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = "attn_tc_kernel") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         p = os.path.join(ROOT, "mla_latent_kv_lat_gb300", "csrc", f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -88,7 +90,7 @@ def recorded_traffic(kernel: str, workload: str):
         rec = json.load(open(p)).get(f"{kernel}:{workload}")
     except Exception:
         return None
-    if not rec or rec.get("kernel_hash") != kernel_hash():
+    if not rec or rec.get("kernel_hash") != kernel_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
