@@ -108,6 +108,18 @@ class ClockSampler:
         self.proc = None
         self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
 
+    def _samples(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def _wait_for(self, n: int, limit_s: float):
+        t0 = time.perf_counter()
+        while self._samples() < n and time.perf_counter() - t0 < limit_s:
+            time.sleep(0.02)
+
     def __enter__(self):
         try:
             self.f = open(self.path, "w")
@@ -116,10 +128,15 @@ class ClockSampler:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        if self.proc is not None:
+            # a timed region shorter than the 200 ms period is still bracketed
+            # by a sample before it and one after it
+            self._wait_for(1, 3.0)
         return self
 
     def __exit__(self, *a):
         if self.proc is not None:
+            self._wait_for(self._samples() + 1, 1.0)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
