@@ -150,6 +150,21 @@ def late_decompress(o_lat, wv_b):
     return np.einsum("thc,hce->the", _f64(o_lat), _f64(wv_b), optimize=True)
 
 
+def output_projection(o, w_o):
+    """The step after the path ([MLA] sec. 4, the einsum ``hdD,bhqd->bqD``):
+    u[t, D] = sum_h sum_d w_o[h, d, D] * o[t, h, d], with o the per-head output
+    [T, H, 128] of late decompression and w_o [H, 128, hidden] (the pages' own
+    layout of W_O).  float64."""
+    return np.einsum("hdD,thd->tD", _f64(w_o), _f64(o), optimize=True)
+
+
+def projected_weights(wv_b, w_o):
+    """W_O folded into W_UV per head ([MLA] sec. 6, the offline pre-absorption
+    the page weighs and rejects as slower): m[h, c, D] = sum_d wv_b[h, c, d] *
+    w_o[h, d, D], so that u = sum_h o_lat[:, h, :] . m[h]."""
+    return np.einsum("hcd,hdD->hcD", _f64(wv_b), _f64(w_o), optimize=True)
+
+
 def attention_absorbed(q_nope, q_pe, c_kv, k_pe, wk_b, wv_b, q_pos, scale: float):
     """The whole absorbed chain: absorb -> latent attention -> late decompression."""
     q_lat = absorb_q(q_nope, wk_b)

@@ -99,3 +99,16 @@ def test_rope_mistakes_are_caught(monkeypatch, which):
         except AssertionError:
             failed += 1
     assert failed >= 1
+
+
+def test_output_projection_mistakes_are_caught(monkeypatch):
+    """Summing over the wrong axis (d of W_O against the token axis) or
+    dropping the head sum, planted in a copy of the oracle's projection, fails
+    the projection pins."""
+    import tests.test_oracle_pins as P
+
+    for bad in (lambda o, w: np.einsum("hdD,thd->tD", np.asarray(w)[:, ::-1], np.asarray(o)),
+                lambda o, w: np.einsum("hdD,thd->tD", np.asarray(w)[:1], np.asarray(o)[:, :1])):
+        monkeypatch.setattr(O, "output_projection", bad)
+        with pytest.raises(AssertionError):
+            P.test_output_projection_matches_brute_force_loops()

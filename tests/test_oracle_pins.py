@@ -346,3 +346,37 @@ def test_cache_rows_keep_the_latent_part_and_rotate_the_rope_part():
     assert np.array_equal(rows[:, :512], c)
     assert np.array_equal(rows[0, 512:], kp[0])
     assert np.array_equal(rows[1:, 512:], O.rope_rotate(kp[1:], pos[1:], 10000.0, 0.025))
+
+
+# ---------------------------------------------------------------------------
+# The step after the path: the output projection (method page sec. 4, the
+# einsum 'hdD,bhqd->bqD'; sec. 6 on folding W_O into W_UV)
+# ---------------------------------------------------------------------------
+def test_output_projection_matches_brute_force_loops():
+    rng = np.random.default_rng(12)
+    T, H, d, D = 3, 2, 4, 5
+    o, w = rng.standard_normal((T, H, d)), rng.standard_normal((H, d, D))
+    ref = np.zeros((T, D))
+    for t in range(T):
+        for n in range(D):
+            ref[t, n] = sum(w[h, k, n] * o[t, h, k] for h in range(H) for k in range(d))
+    np.testing.assert_allclose(O.output_projection(o, w), ref, atol=1e-12)
+
+
+def test_output_projection_is_the_pages_einsum_and_folds_into_wv_b():
+    # the page's own einsum on its [b, h, q, d] layout gives the same u; folding
+    # W_O into W_UV per head (sec. 6) gives the same u from o_lat (associativity)
+    rng = np.random.default_rng(13)
+    T, H, L, d, D = 4, 3, 16, 8, 6
+    o_lat, wv, wo = rng.standard_normal((T, H, L)), rng.standard_normal((H, L, d)), rng.standard_normal((H, d, D))
+    o = O.late_decompress(o_lat, wv)
+    u = O.output_projection(o, wo)
+    page = np.einsum("hdD,bhqd->bqD", wo, o.transpose(1, 0, 2)[None])[0]
+    np.testing.assert_allclose(u, page, atol=1e-12)
+    folded = np.einsum("thc,hcD->tD", o_lat, O.projected_weights(wv, wo))
+    np.testing.assert_allclose(u, folded, atol=1e-10)
+    # one head's weights zero: that head drops out of the sum
+    wo0 = wo.copy()
+    wo0[1] = 0
+    np.testing.assert_allclose(O.output_projection(o, wo0),
+                               O.output_projection(o[:, [0, 2]], wo[[0, 2]]), atol=1e-12)
