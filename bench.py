@@ -266,6 +266,16 @@ def time_steps(torch, step, steps, warmup, flush):
     return step_ms, attn_ms
 
 
+def max_over_ranks(value: float, torch, dist, device: str) -> float:
+    """The slowest rank's value (N replicas: the job ends when the last one
+    does); the value itself without a process group."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, torch, dist, rank, world):
     import mla_latent_kv_lat_gb300 as mla
     from mla_latent_kv_lat_gb300 import build
@@ -288,11 +298,7 @@ def run_ours(args, torch, dist, rank, world):
     err = mla.mla_get_device_error()
     if err != 0:
         raise RuntimeError(f"device error {err} during the bench")
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), torch, dist, "cuda")
     ms_step = total_ms / args.steps
     attn_avg = sum(attn_ms) / len(attn_ms)
     if wl.kind == "prefill":
