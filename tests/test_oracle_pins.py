@@ -380,3 +380,17 @@ def test_output_projection_is_the_pages_einsum_and_folds_into_wv_b():
     wo0[1] = 0
     np.testing.assert_allclose(O.output_projection(o, wo0),
                                O.output_projection(o[:, [0, 2]], wo[[0, 2]]), atol=1e-12)
+
+
+def test_rope_constants_are_the_pages_printed_values():
+    # the cache-append defaults (binding and bench) are the printed freq_base /
+    # freq_scale of the DeepSeek-V3 run, over the printed n_rot = 64 dims
+    import inspect
+
+    from mla_latent_kv_lat_gb300 import binding
+    g = json.load(open(os.path.join(GOLDEN, "page_accounting.json")))
+    items = {it["name"]: it for it in g["items"]}
+    sig = inspect.signature(binding.mla_rope_append).parameters
+    assert sig["freq_base"].default == items["rope_freq_base"]["value"]
+    assert sig["freq_scale"].default == items["rope_freq_scale"]["value"]
+    assert O.QK_ROPE == items["rope_n_rot"]["value"]
