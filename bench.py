@@ -530,6 +530,56 @@ def run_reference(args):
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def sweep_decode(args, torch):
+    """Decode attention (+ combine) of 32 sequences x 128 heads at a range of
+    cache lengths, bf16 and q8_0 cache (the llama-sweep-bench way of reading
+    a decode kernel: throughput against N_KV).  Seeded device-side N(0,1)
+    inputs; one JSON line per point.  Not part of the default bench line."""
+    import mla_latent_kv_lat_gb300 as mla
+    from mla_latent_kv_lat_gb300 import build
+    from mla_latent_kv_lat_gb300 import pipeline as P
+    build.build()
+    mla.load_library()
+    pk, pk_kind = peaks()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+    B, H = 32, 128
+    out = []
+    for L in (1024, 4096, 16384, 32768, 65536):
+        n = B * L
+        kv = torch.randn(n, 576, device="cuda", generator=g).to(torch.bfloat16)
+        kv_q = torch.empty(n, 576, dtype=torch.int8, device="cuda")
+        kv_d = torch.empty(18, n, dtype=torch.float16, device="cuda")
+        mla.mla_quantize_q8_0(kv, kv_q, kv_d)
+        q_lat = torch.randn(B, H, 512, device="cuda", generator=g).to(torch.float16)
+        q_pe = torch.randn(B, H, 64, device="cuda", generator=g).to(torch.bfloat16)
+        seq_len = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        seq_start = torch.arange(B, dtype=torch.int64, device="cuda") * L
+        bufs = P.decode_buffers(B, H, L)
+        for cache, row in (("bf16", 1152), ("q8_0", 612)):
+            def step(stream=None, ev=None):
+                if ev:
+                    ev[0].record()
+                if cache == "bf16":
+                    mla.mla_attn_decode(q_lat, q_pe, kv, seq_start, seq_len, L, bufs.workspace, bufs.o_lat)
+                else:
+                    mla.mla_attn_decode_q8_0(q_lat, q_pe, kv_q, kv_d, seq_start, seq_len, L, bufs.workspace,
+                                             bufs.o_lat)
+                if ev:
+                    ev[1].record()
+            _, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+            ms = sorted(attn_ms)[len(attn_ms) // 2]
+            nbytes = n * row + B * H * (576 + 512) * 2
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out.append({"sweep": "decode", "cache": cache, "B": B, "n_head": H, "cache_len": L,
+                        "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                        "TFLOP/s": round(n * H * FLOP_PER_PAIR_HEAD / (ms * 1e-3) / 1e12, 1)})
+        if mla.mla_get_device_error() != 0:
+            raise RuntimeError("device error during the decode sweep")
+        del kv, kv_q, kv_d
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,6 +589,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-decode", dest="with_decode", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep-decode", action="store_true",
+                    help="instead of the bench line: decode throughput against cache length (one JSON line each)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -550,6 +602,10 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     import torch
+    if args.sweep_decode:
+        for row in sweep_decode(args, torch):
+            print(json.dumps(row), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
