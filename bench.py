@@ -580,6 +580,45 @@ def sweep_decode(args, torch):
     return out
 
 
+def sweep_prefill(args, torch):
+    """Prefill attention (staging included) against chunk length: the Lite
+    shape (16 heads) causal over its own cache, and the V3 shape (128 heads)
+    at position 32768 over a cache ending with the chunk.  Seeded device-side
+    N(0,1) inputs; one JSON line per point.  Not part of the default line."""
+    import mla_latent_kv_lat_gb300 as mla
+    from mla_latent_kv_lat_gb300 import build
+    build.build()
+    mla.load_library()
+    pk, pk_kind = peaks()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(0)
+    out = []
+    points = [(16, T, 0) for T in (1024, 2048, 4096, 8192, 16384)] + [(128, T, 32768) for T in (512, 1024, 2048, 4096)]
+    for H, T, q_pos0 in points:
+        n_kv = q_pos0 + T
+        kv = torch.randn(n_kv, 576, device="cuda", generator=g).to(torch.bfloat16)
+        q_lat = torch.randn(T, H, 512, device="cuda", generator=g).to(torch.float16)
+        q_pe = torch.randn(T, H, 64, device="cuda", generator=g).to(torch.bfloat16)
+        o_lat = torch.empty(T, H, 512, dtype=torch.float16, device="cuda")
+        ws = torch.empty(mla.mla_prefill_workspace_size(H, n_kv), dtype=torch.uint8, device="cuda")
+
+        def step(stream=None, ev=None):
+            if ev:
+                ev[0].record()
+            mla.mla_attn_prefill(q_lat, q_pe, kv, q_pos0, o_lat, workspace=ws)
+            if ev:
+                ev[1].record()
+        _, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+        ms = sorted(attn_ms)[len(attn_ms) // 2]
+        flops = float(T * q_pos0 + T * (T + 1) // 2) * H * FLOP_PER_PAIR_HEAD
+        tf = flops / (ms * 1e-3) / 1e12
+        out.append({"sweep": "prefill", "n_head": H, "T": T, "q_pos0": q_pos0, "row_tiles": (T * H + 127) // 128,
+                    "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / pk["bf16_tflops"], 4)})
+        if mla.mla_get_device_error() != 0:
+            raise RuntimeError("device error during the prefill sweep")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -591,6 +630,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-decode", action="store_true",
                     help="instead of the bench line: decode throughput against cache length (one JSON line each)")
+    ap.add_argument("--sweep-prefill", action="store_true",
+                    help="instead of the bench line: prefill throughput against chunk length (one JSON line each)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -602,8 +643,8 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     import torch
-    if args.sweep_decode:
-        for row in sweep_decode(args, torch):
+    if args.sweep_decode or args.sweep_prefill:
+        for row in (sweep_decode if args.sweep_decode else sweep_prefill)(args, torch):
             print(json.dumps(row), flush=True)
         return
     dist = None
