@@ -8,6 +8,12 @@ seeded synthetic tensors of ``workloads.py`` (no dataset), resident in HBM
 when the timed region starts.  L2 (129 MB) is flushed by writing a 512 MB
 buffer before every timed step; only the step itself is inside the CUDA events.
 
+The JSON line's headline is the DeepSeek-V3-shape 8192-query chunk at
+position 32768 (the largest prefill that fits the bf16 cache workloads); every
+other workload follows under "secondary", each with its own roofline of the
+dominant kernel and its end-to-end number (host buffers, copies inside the
+timed region).
+
 ``--impl reference`` times the CPU oracle (the un-absorbed definition in
 numpy fp64) on a bounded sample of the same workload on the host cores.
 """
@@ -31,8 +37,18 @@ sys.path.insert(0, ROOT)
 from mla_latent_kv_lat_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MLA attn TFLOP/s (prefill) & HBM GB/s (decode) on 1 GB300, % of roofline"
-DEFAULT_WORKLOAD = "lite_t4096"
-DECODE_WORKLOAD = "v3_decode_b32"
+# The headline line: the largest single-GPU prefill (DeepSeek-V3 shape, an
+# 8192-query chunk at position 32768).  Every other workload is measured too,
+# each as a secondary entry with its own roofline and end-to-end number.
+DEFAULT_WORKLOAD = "v3_chunk8192_at32768"
+# "<workload>:materialized" is the same chunk through the materialised
+# prefill (per-head K/V decompressed, then standard attention: the pp_opt
+# path); "<workload>:projected" appends the output projection wo to the
+# absorbed path (late decompression in bf16, then u = o . w_o).
+SECONDARY_WORKLOADS = ["lite_t4096", "lite_t256", "v3_decode_b32", "v3_q8_chunk8192_at90112", "v3_q8_decode_b8",
+                       "v3_cache_append_98304", "v3_chunk8192_at32768:materialized", "lite_t4096:materialized",
+                       "v3_q8_chunk8192_at90112:materialized", "v3_chunk8192_at32768:projected",
+                       "lite_t4096:projected"]
 FLOP_PER_PAIR_HEAD = 2 * 576 + 2 * 512          # scores (576-d) + latent weighted sum (512-d)
 # sources whose hash dates the ncu traffic recorded for each kernel
 KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"],
@@ -64,6 +80,21 @@ APPEND_TOKEN_BYTES = (512 + 64) * 2 + 4 + 8 + 576 * 2 + 576 + 18 * 2
 
 def append_bytes(wl: W.Workload) -> float:
     return float(wl.T) * APPEND_TOKEN_BYTES
+
+
+# the materialised prefill's own work: 2*192 + 2*128 FLOPs per visible pair and
+# head, plus decompressing every row it reads (512 -> 128 + 128 per head)
+FLOP_PER_PAIR_HEAD_MATERIALIZED = 2 * 192 + 2 * 128
+
+
+def materialized_flops(wl: W.Workload) -> float:
+    pairs = wl.T * wl.q_pos0 + wl.T * (wl.T + 1) // 2
+    rows = wl.q_pos0 + wl.T
+    return float(pairs) * wl.n_head * FLOP_PER_PAIR_HEAD_MATERIALIZED + float(rows) * wl.n_head * 2 * 512 * 256
+
+
+def wo_flops(wl: W.Workload) -> float:
+    return 2.0 * wl.T * wl.n_head * 128 * wl.hidden
 
 
 def peaks():
@@ -187,6 +218,126 @@ def setup_append(wl, torch):
     return wl, a, d, caches, step, 1
 
 
+def setup_variant(name, variant, torch):
+    """The materialised prefill (one call: prep, decompression, attention) or
+    the absorbed path with the output projection; the events `ev` bracket the
+    materialised call, or the projection alone."""
+    import mla_latent_kv_lat_gb300 as mla
+    from mla_latent_kv_lat_gb300 import pipeline as P
+    wl = W.WORKLOADS[name]
+    x = W.make_inputs(wl)
+
+    def dev(a):
+        return torch.from_numpy(W.to_bf16(a)[1]).view(torch.bfloat16).cuda()
+
+    d = {"q_nope": dev(x.q_nope), "q_pe": dev(x.q_pe), "wk_b": dev(x.wk_b), "wv_b": dev(x.wv_b)}
+    kv = torch.from_numpy(x.kv_rows_bits()).view(torch.bfloat16).cuda()
+    T, H = wl.T, wl.n_head
+    if variant == "materialized":
+        if wl.cache == "q8_0":
+            n = kv.shape[0]
+            d["kv_q"] = torch.empty(n, 576, dtype=torch.int8, device="cuda")
+            d["kv_d"] = torch.empty(18, n, dtype=torch.float16, device="cuda")
+            mla.mla_quantize_q8_0(kv, d["kv_q"], d["kv_d"])     # the cache producer, outside the timing
+            del kv
+        else:
+            d["kv"] = kv
+        out = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
+        ws = torch.empty(mla.mla_prefill_materialized_workspace_size(H, T, wl.q_pos0), dtype=torch.uint8,
+                         device="cuda")
+
+        def step(stream=None, ev=None):
+            if ev:
+                ev[0].record()
+            if wl.cache == "q8_0":
+                mla.mla_attn_prefill_materialized_q8_0(d["q_nope"], d["q_pe"], d["kv_q"], d["kv_d"], d["wk_b"],
+                                                       d["wv_b"], wl.q_pos0, out, workspace=ws, stream=stream)
+            else:
+                mla.mla_attn_prefill_materialized(d["q_nope"], d["q_pe"], d["kv"], d["wk_b"], d["wv_b"], wl.q_pos0,
+                                                  out, workspace=ws, stream=stream)
+            if ev:
+                ev[1].record()
+        return wl, x, d, (out, ws), step, 3
+    d["kv"] = kv
+    d["w_o"] = dev(W.make_wo(H, wl.hidden))
+    bufs = P.prefill_buffers(T, H, n_kv=x.n_rows)
+    pb = P.project_buffers(T, H, wl.hidden)
+
+    def step(stream=None, ev=None):
+        mla.mla_absorb_q(d["q_nope"], d["wk_b"], bufs.q_lat, stream=stream)
+        mla.mla_attn_prefill(bufs.q_lat, d["q_pe"], d["kv"], wl.q_pos0, bufs.o_lat, stream=stream,
+                             workspace=bufs.workspace)
+        mla.mla_late_decompress_bf16(bufs.o_lat, d["wv_b"], pb.o16, stream=stream)
+        if ev:
+            ev[0].record()
+        mla.mla_output_project(pb.o16, d["w_o"], pb.u, stream=stream)
+        if ev:
+            ev[1].record()
+    return wl, x, d, (bufs, pb), step, 5
+
+
+def measure_variant(args, torch, full, flush, pk, pk_kind, world=1):
+    name, variant = full.split(":")
+    wl, x, d, bufs, step, launches = setup_variant(name, variant, torch)
+    torch.cuda.synchronize()
+    step_ms, ev_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+    ms = sum(step_ms) / len(step_ms)
+    kms = sum(ev_ms) / len(ev_ms)
+    peak = pk["bf16_tflops"]
+    out = {"workload": full, "ms_per_step": round(ms, 4), "tokens_per_s": round(wl.T * world / (ms * 1e-3), 1),
+           "gpu_launches": launches * args.steps}
+    if variant == "materialized":
+        own = materialized_flops(wl) / (kms * 1e-3) / 1e12
+        out.update({"value": round(materialized_flops(wl) * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "value_of": "own work: pairs x H x 640 + rows x H x 262144 (decompression)",
+                    "absorbed_equiv_tflops": round(attn_flops(wl, x) * world / (ms * 1e-3) / 1e12, 3),
+                    "roofline": {"bound": "tensor", "achieved": round(own, 3), "peak": peak, "unit": "TFLOP/s",
+                                 "frac": round(own / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst",
+                                 "kernel": "pp_prep_kernel+pp_decompress_tc_kernel+pp_attn_tc_kernel",
+                                 "attn_ms": round(kms, 4), "traffic": None}})
+        out["e2e"] = e2e_generic(args, torch, d, step, bufs[0], materialized_flops(wl), 1e12, "TFLOP/s")
+    else:
+        tf = wo_flops(wl) / (kms * 1e-3) / 1e12
+        out.update({"value": round(attn_flops(wl, x) * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "value_of": "absorbed attention FLOPs per step, the step now ending with u = o . w_o",
+                    "hidden": wl.hidden,
+                    "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak, "unit": "TFLOP/s",
+                                 "frac": round(tf / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst",
+                                 "kernel": "wo_gemm_tc_kernel", "attn_ms": round(kms, 4), "traffic": None,
+                                 "flops": wo_flops(wl)}})
+    del d, bufs, step
+    return out
+
+
+def e2e_generic(args, torch, d, step, out_dev, units, scale, unit):
+    """One call through the public entry point per step, its inputs copied from
+    pinned host memory first and its output copied back after."""
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+    def one():
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    return {"value": round(units / (ms * 1e-3) / scale, 3), "unit": unit, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+
 def setup_workload(name, torch):
     import mla_latent_kv_lat_gb300 as mla
     from mla_latent_kv_lat_gb300 import pipeline as P
@@ -276,6 +427,63 @@ def max_over_ranks(value: float, torch, dist, device: str) -> float:
     return float(t.item())
 
 
+def roofline_of(wl, x, attn_ms, pk, pk_kind):
+    """Roofline of the step's dominant kernel (the attention kernel, with the
+    decode combine; the append kernel) from its measured average duration."""
+    if wl.kind == "prefill":
+        ach = attn_flops(wl, x) / (attn_ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst"}
+        if "bf16_tflops_sustained" in pk:
+            roof["frac_of_sustained"] = round(ach / pk["bf16_tflops_sustained"], 4)
+    else:
+        units = append_bytes(wl) if wl.kind == "append" else decode_bytes(wl, x)
+        ach = units / (attn_ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} HBM copy"}
+        if wl.kind == "decode":
+            tf = attn_flops(wl, x) / (attn_ms * 1e-3) / 1e12
+            roof["tensor_tflops"] = round(tf, 2)
+            roof["tensor_frac"] = round(tf / pk["bf16_tflops"], 4)
+    kname = "rope_append_kernel" if wl.kind == "append" else "attn_tc_kernel"
+    roof["traffic"] = recorded_traffic(kname, wl.name)
+    roof["kernel"] = kname if wl.kind != "decode" else "attn_tc_kernel+combine_kernel"
+    roof["attn_ms"] = round(attn_ms, 4)
+    return roof
+
+
+def measure(args, torch, name, flush, pk, pk_kind, world=1, with_e2e=True):
+    """Time `steps` whole steps of one workload (after `warmup` untimed ones),
+    L2 flushed before each; returns the per-workload figures, the live inputs
+    and the raw per-step times."""
+    wl, x, d, bufs, step, launches = setup_workload(name, torch)
+    torch.cuda.synchronize()
+    step_ms, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
+    ms = sum(step_ms) / len(step_ms)
+    attn = sum(attn_ms) / len(attn_ms)
+    if wl.kind == "prefill":
+        value, unit = attn_flops(wl, x) * world / (ms * 1e-3) / 1e12, "TFLOP/s"
+    else:
+        units = append_bytes(wl) if wl.kind == "append" else decode_bytes(wl, x)
+        value, unit = units * world / (ms * 1e-3) / 1e9, "GB/s"
+    out = {"workload": wl.name, "value": round(value, 3), "unit": unit, "ms_per_step": round(ms, 4),
+           "roofline": roofline_of(wl, x, attn, pk, pk_kind), "gpu_launches": launches * args.steps}
+    if wl.kind == "prefill":
+        out["tokens_per_s"] = round(wl.T / (ms * 1e-3), 1)
+    elif wl.kind == "decode":
+        out["tokens_per_s"] = round(wl.B / (ms * 1e-3), 1)
+    if with_e2e:
+        if wl.kind == "prefill":
+            out["e2e"] = e2e_prefill(args, torch, wl, x, d, bufs)
+        elif wl.kind == "append":
+            out["e2e"] = e2e_append(args, torch, wl, d, bufs)
+        else:
+            out["e2e"] = e2e_decode(args, torch, wl, x, d, bufs)
+    return out, (wl, x), sum(step_ms)
+
+
 def run_ours(args, torch, dist, rank, world):
     import mla_latent_kv_lat_gb300 as mla
     from mla_latent_kv_lat_gb300 import build
@@ -287,6 +495,7 @@ def run_ours(args, torch, dist, rank, world):
     pk, pk_kind = peaks()
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
 
+    # the headline workload: clocks sampled during its timed steps
     wl, x, d, bufs, step, launches = setup_workload(args.workload, torch)
     if dist is not None:
         dist.barrier()
@@ -302,25 +511,10 @@ def run_ours(args, torch, dist, rank, world):
     ms_step = total_ms / args.steps
     attn_avg = sum(attn_ms) / len(attn_ms)
     if wl.kind == "prefill":
-        units = attn_flops(wl, x)
-        value = units * world / (ms_step * 1e-3) / 1e12
-        unit = "TFLOP/s"
-        ach = attn_flops(wl, x) / (attn_avg * 1e-3) / 1e12
-        peak = pk["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst"}
+        value, unit = attn_flops(wl, x) * world / (ms_step * 1e-3) / 1e12, "TFLOP/s"
     else:
         units = append_bytes(wl) if wl.kind == "append" else decode_bytes(wl, x)
-        value = units * world / (ms_step * 1e-3) / 1e9
-        unit = "GB/s"
-        ach = units / (attn_avg * 1e-3) / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_kind": f"{pk_kind} HBM copy"}
-    kname = "rope_append_kernel" if wl.kind == "append" else "attn_tc_kernel"
-    roof["traffic"] = recorded_traffic(kname, wl.name)
-    roof["kernel"] = kname
-    roof["attn_ms"] = round(attn_avg, 4)
+        value, unit = units * world / (ms_step * 1e-3) / 1e9, "GB/s"
 
     out = {"metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
@@ -330,33 +524,48 @@ def run_ours(args, torch, dist, rank, world):
                       "T": wl.T, "q_pos0": wl.q_pos0, "n_kv": wl.n_kv, "B": wl.B,
                       "parallelism": "replicas" if world > 1 else "single GPU",
                       "l2": "flushed before every step (512 MB write)"},
-           "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clk.summary(),
-           "wall_s_timed": round(t_wall, 3)}
+           "roofline": roofline_of(wl, x, attn_avg, pk, pk_kind), "gpu_launches": launches * args.steps,
+           "clocks": clk.summary(), "wall_s_timed": round(t_wall, 3)}
     if wl.kind == "prefill":
+        out["tokens_per_s"] = round(wl.T * world / (ms_step * 1e-3), 1)
         out["e2e"] = e2e_prefill(args, torch, wl, x, d, bufs)
     elif wl.kind == "append":
         out["e2e"] = e2e_append(args, torch, wl, d, bufs)
     else:
         out["e2e"] = e2e_decode(args, torch, wl, x, d, bufs)
-    if args.with_decode and wl.kind == "prefill":
-        out["decode"] = secondary(args, torch, DECODE_WORKLOAD, flush, pk, pk_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, x, unit, budget_s=args.cpu_budget)
+    del d, bufs, step
+    torch.cuda.empty_cache()
+
+    # every other workload, one after the other (replicas: each rank its own)
+    names = [n for n in secondary_names(args) if n != wl.name]
+    if names:
+        out["secondary"] = {}
+        for name in names:
+            if ":" in name:
+                sec = measure_variant(args, torch, name, flush, pk, pk_kind, world)
+            else:
+                sec, _, _ = measure(args, torch, name, flush, pk, pk_kind, world)
+            if mla.mla_get_device_error() != 0:
+                raise RuntimeError(f"device error during the {name} bench")
+            out["secondary"][name] = sec
+            out["gpu_launches"] += sec["gpu_launches"]
+            torch.cuda.empty_cache()
     return out
 
 
-def secondary(args, torch, name, flush, pk, pk_kind):
-    wl, x, d, bufs, step, launches = setup_workload(name, torch)
-    step_ms, attn_ms = time_steps(torch, step, args.steps, args.warmup, flush)
-    ms = sum(step_ms) / len(step_ms)
-    attn = sum(attn_ms) / len(attn_ms)
-    gbs = decode_bytes(wl, x) / (ms * 1e-3) / 1e9
-    ach = decode_bytes(wl, x) / (attn * 1e-3) / 1e9
-    return {"workload": name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
-            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(ach / pk["hbm_gbs"], 4), "peak_kind": f"{pk_kind} HBM copy",
-                         "attn_ms": round(attn, 4), "kernel": "attn_tc_kernel+combine_kernel"},
-            "tflops": round(attn_flops(wl, x) / (attn * 1e-3) / 1e12, 2)}
+def secondary_names(args):
+    if args.secondary == "none":
+        return []
+    if args.secondary == "all":
+        return list(SECONDARY_WORKLOADS)
+    names = [n for n in args.secondary.split(",") if n]
+    for n in names:
+        base, _, variant = n.partition(":")
+        if base not in W.WORKLOADS or variant not in ("", "materialized", "projected"):
+            raise SystemExit(f"unknown workload {n}")
+    return names
 
 
 def e2e_prefill(args, torch, wl, x, d, bufs):
@@ -626,7 +835,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
-    ap.add_argument("--no-decode", dest="with_decode", action="store_false")
+    ap.add_argument("--secondary", default="all",
+                    help="workloads measured after the headline one: all (default), none, or a comma list")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-decode", action="store_true",
                     help="instead of the bench line: decode throughput against cache length (one JSON line each)")

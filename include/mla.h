@@ -29,6 +29,14 @@
  *   converted on load, exactly for values inside the fp16 range), because
  *   rounding q_lat, P and o_lat to bf16 alone would cost about 2.8e-3 mean
  *   relative error of o, against about 0.6e-3 with fp16.
+ * - fp16 range.  Where a bf16 value (cache row, q_pe) or an fp32 result
+ *   (q_lat) becomes an fp16 operand, a magnitude of 65536 or more (bf16
+ *   values between 65504 and 65536 do not exist), an infinity or a NaN is
+ *   recorded as MLA_ERR_RANGE in the device error word; for a q8_0 cache the
+ *   check is a block scale of 516 or more (127 x 516 > 65504).  A row whose
+ *   partial score (before the softmax scale) exceeds 65504 in magnitude is
+ *   recorded the same way when it makes the row maximum infinite or NaN.  The
+ *   affected outputs are not defined; the others are computed as usual.
  * - Every device pointer must be 16-byte aligned (MLA_ERR_MISALIGNED).
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Work is enqueued asynchronously on it; host arguments are
@@ -36,6 +44,10 @@
  *   at once with nothing launched.
  * - Return value: MLA_OK or a negative mla_status.  Nothing aborts, traps or
  *   prints.  A launch error reported by the CUDA runtime maps to MLA_ERR_CUDA.
+ * - The device address of the error word (and of the fixed scratch of
+ *   mla_attn_decode_static) is looked up on a device's first call and kept
+ *   for the life of the process: after cudaDeviceReset() on a device, do not
+ *   call the library on that device again in the same process.
  * - Kernels that wait on asynchronous copies or tensor-core work bound every
  *   wait (0.5 s of the GPU's global timer).  A wait that runs out records
  *   MLA_ERR_TIMEOUT in a per-device error word, abandons its tile and
@@ -84,7 +96,8 @@ typedef enum mla_status {
   MLA_ERR_MISALIGNED = -3,   /* a device pointer is not 16-byte aligned        */
   MLA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required     */
   MLA_ERR_CUDA = -5,         /* the CUDA runtime reported an error             */
-  MLA_ERR_TIMEOUT = -6       /* a device-side bounded wait ran out             */
+  MLA_ERR_TIMEOUT = -6,      /* a device-side bounded wait ran out             */
+  MLA_ERR_RANGE = -7         /* a value fp16 cannot hold met an fp16 operand   */
 } mla_status;
 
 /* Step 1, K absorption (method page sec. 3 and the q_nope2 line of sec. 4):
@@ -131,6 +144,50 @@ int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q
                           int32_t T, int32_t q_pos0, void* workspace, size_t ws_bytes,
                           void* o_lat, float* lse, void* stream);
 
+/* Bytes of device workspace mla_attn_prefill_materialized needs for a chunk
+ * of T queries at positions q_pos0.. with head_chunk heads decompressed at a
+ * time (0 = all n_head): fp16 queries (T rounded up to 128, x H x 384 bytes),
+ * fp16 RoPE keys (128 bytes a row), for one head chunk fp16 keys and values
+ * (512 bytes a row and head), and for a q8_0 cache an fp16 copy of its rows
+ * (1152 bytes a row), for the q_pos0 + T rows a chunk reads.  The size serves
+ * either cache type.  Returns 0 for invalid arguments.                        */
+size_t mla_prefill_materialized_workspace_size(const mla_dims* dims, int32_t T, int32_t q_pos0,
+                                               int32_t head_chunk);
+
+/* The materialised prefill ("pp_opt", method page sec. 8.4): for a long chunk
+ * the keys and values of every visible row are decompressed from the latent
+ * cache per head, once per call, and standard causal attention runs on them:
+ *   k[j][h] = [ wk_b[h] c_kv[j] (128) | k_pe[j] (64) ],  v[j][h] = wv_b[h]^T c_kv[j]
+ *   q[t][h] = [ q_nope[t][h] | q_pe[t][h] ]
+ *   o[t][h] = sum_j softmax_j(scale * q[t][h] . k[j][h]) v[j][h],  j <= q_pos0 + t
+ * (the un-absorbed definition of the method page, sec. 1, computed directly:
+ * 640 FLOPs per visible pair and head instead of the absorbed 2176, plus the
+ * decompression).  No late decompression follows: o is the per-head output.
+ * q_nope device bf16 [T][H][128]; q_pe device bf16 [T][H][64]
+ * kv     device bf16 [n_kv][576] latent cache; wk_b bf16 [H][128][512];
+ *        wv_b bf16 [H][512][128]
+ * head_chunk  heads decompressed at a time (0 = all): bounds the workspace the
+ *        way ik_llama.cpp's -amb option bounds its attention buffers
+ * workspace device, ws_bytes >= mla_prefill_materialized_workspace_size(...)
+ * o      device fp32 [T][H][128] output;  lse fp32 [T][H] or NULL
+ * Requires T >= 1, q_pos0 >= 0, q_pos0 + T <= n_kv; rows past q_pos0 + T - 1
+ * are never read.  Keys, values, queries and probabilities are fp16 tensor-
+ * core operands (fp32 accumulation); the fp16 range rules above apply.        */
+int mla_attn_prefill_materialized(const mla_dims* dims, const void* q_nope, const void* q_pe,
+                                  const void* kv, const void* wk_b, const void* wv_b, int32_t n_kv,
+                                  int32_t T, int32_t q_pos0, int32_t head_chunk, void* workspace,
+                                  size_t ws_bytes, float* o, float* lse, void* stream);
+
+/* As mla_attn_prefill_materialized over a q8_0 latent cache (kv_q int8
+ * [n_kv][576], kv_d fp16 [18][n_kv]; method page sec. 8.1 and 8.4): the rows
+ * read are first dequantised to fp16 (scale x code, the values every q8_0
+ * entry point uses), then decompressed with the weights converted to fp16.   */
+int mla_attn_prefill_materialized_q8_0(const mla_dims* dims, const void* q_nope, const void* q_pe,
+                                       const int8_t* kv_q, const uint16_t* kv_d, const void* wk_b,
+                                       const void* wv_b, int32_t n_kv, int32_t T, int32_t q_pos0,
+                                       int32_t head_chunk, void* workspace, size_t ws_bytes, float* o,
+                                       float* lse, void* stream);
+
 /* Bytes of device workspace mla_attn_decode / mla_attn_decode_q8_0 need for
  * B sequences (split-KV partial results): the keys of all sequences are split
  * evenly over G = (SM count / 2) clusters, which makes at most B + G - 1
@@ -149,8 +206,12 @@ size_t mla_decode_workspace_size(const mla_dims* dims, int32_t B, int32_t max_le
  * seq_len    device int32 [B]  1 <= seq_len[b] <= max_len, rows inside kv
  * workspace  device, ws_bytes >= mla_decode_workspace_size(dims, B, max_len)
  * o_lat      device fp16 [B][H][512]  output
- * n_rows is the row count of kv (used for argument checks and the q8_0
- * scale layout).  seq_start/seq_len are read on the device only.              */
+ * n_rows is the row count of kv (the q8_0 scale stride, and the bound of the
+ * rows a sequence may name).  seq_start/seq_len are read on the device only:
+ * a sequence with seq_len[b] < 1, seq_len[b] > max_len, seq_start[b] < 0 or
+ * seq_start[b] + seq_len[b] > n_rows is skipped (no row of it is read and its
+ * o_lat rows are left as they were) and recorded as MLA_ERR_INVALID_ARG in
+ * the device error word; the other sequences are computed as usual.           */
 int mla_attn_decode(const mla_dims* dims, const void* q_lat, const void* q_pe,
                     const void* kv, int64_t n_rows, const int64_t* seq_start,
                     const int32_t* seq_len, int32_t B, int32_t max_len,
@@ -198,6 +259,23 @@ int mla_attn_decode_static(const mla_dims* dims, const void* q_lat, const void* 
 int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b,
                         float* o, int32_t T, void* stream);
 
+/* As mla_late_decompress, with o rounded once to bf16 (the type the output
+ * projection below takes): o device bf16 [T][H][128].                         */
+int mla_late_decompress_bf16(const mla_dims* dims, const void* o_lat, const void* wv_b,
+                             void* o, int32_t T, void* stream);
+
+/* The step after the path, the attention output projection (method page
+ * sec. 4: the heads' outputs, flattened to H * 128, times wo -- the einsum
+ * hdD,bhqd->bqD; the V up-projection stays a separate, earlier step):
+ *   u[t][n] = sum_h sum_e o[t][h][e] * w_o[h][e][n]
+ * o    device bf16 [T][H][128]   (mla_late_decompress_bf16's output)
+ * w_o  device bf16 [H][128][D]   (row-major [H*128][D])
+ * u    device fp32 [T][D]        output, fp32 accumulation
+ * T >= 1; D (the hidden size) a multiple of 64, at most 1<<20
+ * (MLA_ERR_UNSUPPORTED otherwise).  A dense GEMM on the tensor cores.         */
+int mla_output_project(const mla_dims* dims, const void* o, const void* w_o, float* u,
+                       int32_t T, int32_t D, void* stream);
+
 /* Quantise n bf16 cache rows [n][576] to the q8_0 layout above (the producer
  * of the sec. 8.1 cache).  Per block: amax = max |x|, d = amax / 127 (fp32),
  * q = round-half-away-from-zero(x / d) clamped to [-127, 127] (0 when
@@ -234,10 +312,11 @@ int mla_rope_append(const void* c_kv, const void* k_pe, const int32_t* pos, cons
                     uint16_t* kv_d, int64_t ld_d, int64_t n_rows, void* stream);
 
 /* Synchronise `stream`, then return and clear the current device's error
- * word: MLA_OK, or the first device-side error (MLA_ERR_TIMEOUT from a
- * bounded wait, MLA_ERR_INVALID_ARG from mla_rope_append's slot check)
- * recorded since the last call.  MLA_ERR_CUDA if the synchronisation itself
- * fails.                                                                      */
+ * word: MLA_OK, or the first device-side error recorded since the last call
+ * (MLA_ERR_TIMEOUT from a bounded wait, MLA_ERR_INVALID_ARG from the slot
+ * check of mla_rope_append or the sequence check of the decodes,
+ * MLA_ERR_RANGE from an fp16 conversion).  MLA_ERR_CUDA if the
+ * synchronisation itself fails.                                               */
 int mla_get_device_error(void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an

@@ -21,7 +21,7 @@ KV_LORA_RANK, QK_ROPE, QK_NOPE, V_HEAD, ROW = 512, 64, 128, 128, 576
 Q8_BLOCKS = 18
 
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_MISALIGNED",
-          -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_CUDA", -6: "MLA_ERR_TIMEOUT"}
+          -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_CUDA", -6: "MLA_ERR_TIMEOUT", -7: "MLA_ERR_RANGE"}
 
 
 class MLAError(RuntimeError):
@@ -50,11 +50,18 @@ _SIGS = {
     "mla_prefill_workspace_size": ([_D, _I32], _SZ),
     "mla_attn_prefill": ([_D, _P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P, _P], ctypes.c_int),
     "mla_attn_prefill_q8_0": ([_D, _P, _P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P, _P], ctypes.c_int),
+    "mla_prefill_materialized_workspace_size": ([_D, _I32, _I32, _I32], _SZ),
+    "mla_attn_prefill_materialized": ([_D, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P, _P],
+                                      ctypes.c_int),
+    "mla_attn_prefill_materialized_q8_0": ([_D, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P,
+                                            _P], ctypes.c_int),
     "mla_decode_workspace_size": ([_D, _I32, _I32], _SZ),
     "mla_attn_decode": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "mla_attn_decode_q8_0": ([_D, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "mla_attn_decode_static": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P], ctypes.c_int),
     "mla_late_decompress": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "mla_late_decompress_bf16": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "mla_output_project": ([_D, _P, _P, _P, _I32, _I32, _P], ctypes.c_int),
     "mla_quantize_q8_0": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "mla_rope_append": ([_P, _P, _P, _P, _I32, ctypes.c_float, ctypes.c_float, _P, _P, _P, _I64, _I64, _P],
                         ctypes.c_int),
@@ -133,6 +140,26 @@ def mla_late_decompress(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor
     _check("mla_late_decompress", load_library().mla_late_decompress(ctypes.byref(d), *args, T, _stream(stream)))
 
 
+def mla_late_decompress_bf16(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor, scale=None, stream=None):
+    T, H = o_lat.shape[0], o_lat.shape[1]
+    d = make_dims(H, scale)
+    args = (_need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)),
+            _need(wv_b, "wv_b", torch.bfloat16, (H, KV_LORA_RANK, V_HEAD)),
+            _need(o, "o", torch.bfloat16, (T, H, V_HEAD)))
+    _check("mla_late_decompress_bf16",
+           load_library().mla_late_decompress_bf16(ctypes.byref(d), *args, T, _stream(stream)))
+
+
+def mla_output_project(o: torch.Tensor, w_o: torch.Tensor, u: torch.Tensor, scale=None, stream=None):
+    """u [T, D] fp32 = o [T, H, 128] bf16 flattened, times w_o [H, 128, D] bf16."""
+    T, H = o.shape[0], o.shape[1]
+    D = w_o.shape[2]
+    d = make_dims(H, scale)
+    args = (_need(o, "o", torch.bfloat16, (T, H, V_HEAD)), _need(w_o, "w_o", torch.bfloat16, (H, V_HEAD, D)),
+            _need(u, "u", torch.float32, (T, D)))
+    _check("mla_output_project", load_library().mla_output_project(ctypes.byref(d), *args, T, D, _stream(stream)))
+
+
 def mla_prefill_workspace_size(n_head: int, n_kv: int, scale=None) -> int:
     d = make_dims(n_head, scale)
     return int(load_library().mla_prefill_workspace_size(ctypes.byref(d), n_kv))
@@ -171,6 +198,54 @@ def mla_attn_prefill_q8_0(q_lat, q_pe, kv_q, kv_d, q_pos0: int, o_lat, lse=None,
         _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_kv)), n_kv, T, q_pos0, wp, wn,
         _need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)), lp, _stream(stream))
     _check("mla_attn_prefill_q8_0", st)
+
+
+def mla_prefill_materialized_workspace_size(n_head: int, T: int, q_pos0: int, head_chunk: int = 0,
+                                            scale=None) -> int:
+    d = make_dims(n_head, scale)
+    return int(load_library().mla_prefill_materialized_workspace_size(ctypes.byref(d), T, q_pos0, head_chunk))
+
+
+def mla_attn_prefill_materialized(q_nope, q_pe, kv, wk_b, wv_b, q_pos0: int, o, lse=None, head_chunk: int = 0,
+                                  workspace=None, scale=None, stream=None):
+    """o [T, H, 128] fp32 by decompressing the visible cache rows per head and
+    running standard causal attention on them (the pp_opt prefill)."""
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    n_kv = kv.shape[0]
+    d = make_dims(H, scale)
+    if workspace is None:
+        workspace = torch.empty(mla_prefill_materialized_workspace_size(H, T, q_pos0, head_chunk, scale),
+                                dtype=torch.uint8, device=kv.device)
+    lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
+    st = load_library().mla_attn_prefill_materialized(
+        ctypes.byref(d), _need(q_nope, "q_nope", torch.bfloat16, (T, H, QK_NOPE)),
+        _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv, "kv", torch.bfloat16, (n_kv, ROW)),
+        _need(wk_b, "wk_b", torch.bfloat16, (H, QK_NOPE, KV_LORA_RANK)),
+        _need(wv_b, "wv_b", torch.bfloat16, (H, KV_LORA_RANK, V_HEAD)), n_kv, T, q_pos0, head_chunk,
+        _need(workspace, "workspace", torch.uint8), workspace.numel(), _need(o, "o", torch.float32, (T, H, V_HEAD)),
+        lp, _stream(stream))
+    _check("mla_attn_prefill_materialized", st)
+
+
+def mla_attn_prefill_materialized_q8_0(q_nope, q_pe, kv_q, kv_d, wk_b, wv_b, q_pos0: int, o, lse=None,
+                                       head_chunk: int = 0, workspace=None, scale=None, stream=None):
+    """The materialised prefill over a q8_0 cache (kv_q int8 [n, 576], kv_d fp16 [18, n])."""
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    n_kv = kv_q.shape[0]
+    d = make_dims(H, scale)
+    if workspace is None:
+        workspace = torch.empty(mla_prefill_materialized_workspace_size(H, T, q_pos0, head_chunk, scale),
+                                dtype=torch.uint8, device=kv_q.device)
+    lp = _need(lse, "lse", torch.float32, (T, H)) if lse is not None else None
+    st = load_library().mla_attn_prefill_materialized_q8_0(
+        ctypes.byref(d), _need(q_nope, "q_nope", torch.bfloat16, (T, H, QK_NOPE)),
+        _need(q_pe, "q_pe", torch.bfloat16, (T, H, QK_ROPE)), _need(kv_q, "kv_q", torch.int8, (n_kv, ROW)),
+        _need(kv_d, "kv_d", torch.float16, (Q8_BLOCKS, n_kv)),
+        _need(wk_b, "wk_b", torch.bfloat16, (H, QK_NOPE, KV_LORA_RANK)),
+        _need(wv_b, "wv_b", torch.bfloat16, (H, KV_LORA_RANK, V_HEAD)), n_kv, T, q_pos0, head_chunk,
+        _need(workspace, "workspace", torch.uint8), workspace.numel(), _need(o, "o", torch.float32, (T, H, V_HEAD)),
+        lp, _stream(stream))
+    _check("mla_attn_prefill_materialized_q8_0", st)
 
 
 def mla_decode_workspace_size(n_head: int, B: int, max_len: int, scale=None) -> int:

@@ -5,6 +5,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 #include "append.cuh"
 #include "kernels.cuh"
 
@@ -15,13 +17,17 @@ __device__ int g_device_error;   // first device-side error since the last read
 
 constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
 
-// Device address of the current device's error word (set up once per device).
+// Device address of the current device's error word (looked up once per
+// device, with that device current; several host threads may make their
+// first call at once).
 cudaError_t error_word(int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_err_mu);
   if (g_err_ptr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
@@ -84,7 +90,7 @@ int prefill_common(const mla_dims* dims, const void* q_lat, const void* q_pe, co
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   const int64_t rows = static_cast<int64_t>(q_pos0) + T;     // rows past the last query are never read
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = launch_stage_cache_f16(q8 ? nullptr : kv, kv_q, kv_d, n_kv, rows, workspace, st);
+  e = launch_stage_cache_f16(q8 ? nullptr : kv, kv_q, kv_d, n_kv, rows, workspace, err, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   AttnTcArgs a = {};
   a.q_lat = q_lat;
@@ -140,6 +146,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   a.seq_start = seq_start;
   a.seq_len = seq_len;
   a.n_seq = B;
+  a.max_len = max_len;
   a.ws_o = static_cast<float*>(workspace);
   a.ws_ml = a.ws_o + slots * kLatent;
   a.err = err;
@@ -150,7 +157,11 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
   CombineArgs c = {};
   c.ws_o = a.ws_o;
   c.ws_ml = a.ws_ml;
+  c.seq_start = seq_start;
   c.seq_len = seq_len;
+  c.n_rows = n_rows;
+  c.max_len = max_len;
+  c.err = err;
   c.o_lat = o_lat;
   c.B = B;
   c.n_head = dims->n_head;
@@ -159,7 +170,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
 }
 
 int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32_t T, int K, int N, bool f32,
-              void* stream) {
+              void* stream, bool out_bf16 = false) {
   int s = check_dims(dims);
   if (s != MLA_OK) return s;
   s = check_ptrs({a, w, c});
@@ -167,7 +178,7 @@ int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32
   if (T < 1) return MLA_ERR_INVALID_ARG;
   int* err = nullptr;
   if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
-  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, f32 ? 1 : 0};
+  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, (f32 || out_bf16) ? 1 : 0, out_bf16 ? 1 : 0};
   return to_status(launch_head_gemm_tc(g, err, kDefaultWaitUs, static_cast<cudaStream_t>(stream)));
 }
 
@@ -186,6 +197,87 @@ int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* wk_b, voi
 int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b, float* o, int32_t T,
                         void* stream) {
   return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, true, stream);
+}
+
+int mla_late_decompress_bf16(const mla_dims* dims, const void* o_lat, const void* wv_b, void* o, int32_t T,
+                             void* stream) {
+  return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, false, stream, true);
+}
+
+size_t mla_prefill_materialized_workspace_size(const mla_dims* dims, int32_t T, int32_t q_pos0, int32_t head_chunk) {
+  if (check_dims(dims) != MLA_OK || T < 1 || q_pos0 < 0 || head_chunk < 0 || head_chunk > dims->n_head) return 0;
+  if (static_cast<int64_t>(q_pos0) + T > INT32_MAX) return 0;
+  // enough for either cache type (a q8_0 cache adds the fp16 staging copy)
+  return pp_workspace_bytes(dims->n_head, T, q_pos0, head_chunk == 0 ? dims->n_head : head_chunk, true);
+}
+
+int materialized_common(const mla_dims* dims, const void* q_nope, const void* q_pe, const void* kv,
+                        const int8_t* kv_q, const uint16_t* kv_d, const void* wk_b, const void* wv_b, int32_t n_kv,
+                        int32_t T, int32_t q_pos0, int32_t head_chunk, void* workspace, size_t ws_bytes, float* o,
+                        float* lse, void* stream) {
+  const bool q8 = kv == nullptr;
+  int s = check_dims(dims);
+  if (s != MLA_OK) return s;
+  s = q8 ? check_ptrs({q_nope, q_pe, kv_q, kv_d, wk_b, wv_b, o}) : check_ptrs({q_nope, q_pe, kv, wk_b, wv_b, o});
+  if (s != MLA_OK) return s;
+  if (lse != nullptr && !aligned16(lse)) return MLA_ERR_MISALIGNED;
+  if (T < 1 || q_pos0 < 0 || n_kv < 1 || head_chunk < 0 || head_chunk > dims->n_head) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(q_pos0) + T > n_kv) return MLA_ERR_INVALID_ARG;
+  const int hc = head_chunk == 0 ? dims->n_head : head_chunk;
+  if (workspace == nullptr || ws_bytes < pp_workspace_bytes(dims->n_head, T, q_pos0, hc, q8)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_MISALIGNED;
+  PpArgs p = {};
+  p.q_nope = q_nope;
+  p.q_pe = q_pe;
+  p.kv = q8 ? nullptr : kv;
+  p.kv_q = kv_q;
+  p.kv_d = kv_d;
+  p.ld_d = n_kv;
+  p.wk_b = wk_b;
+  p.wv_b = wv_b;
+  p.workspace = workspace;
+  p.o = o;
+  p.lse = lse;
+  p.T = T;
+  p.H = dims->n_head;
+  p.q_pos0 = q_pos0;
+  p.hc = hc;
+  p.scale_log2 = dims->scale * kLog2eF;
+  p.wait_us = kDefaultWaitUs;
+  if (error_word(&p.err) != cudaSuccess) return MLA_ERR_CUDA;
+  return to_status(launch_pp_prefill(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_attn_prefill_materialized(const mla_dims* dims, const void* q_nope, const void* q_pe, const void* kv,
+                                  const void* wk_b, const void* wv_b, int32_t n_kv, int32_t T, int32_t q_pos0,
+                                  int32_t head_chunk, void* workspace, size_t ws_bytes, float* o, float* lse,
+                                  void* stream) {
+  if (kv == nullptr) return MLA_ERR_INVALID_ARG;
+  return materialized_common(dims, q_nope, q_pe, kv, nullptr, nullptr, wk_b, wv_b, n_kv, T, q_pos0, head_chunk,
+                             workspace, ws_bytes, o, lse, stream);
+}
+
+int mla_attn_prefill_materialized_q8_0(const mla_dims* dims, const void* q_nope, const void* q_pe,
+                                       const int8_t* kv_q, const uint16_t* kv_d, const void* wk_b, const void* wv_b,
+                                       int32_t n_kv, int32_t T, int32_t q_pos0, int32_t head_chunk, void* workspace,
+                                       size_t ws_bytes, float* o, float* lse, void* stream) {
+  if (kv_q == nullptr || kv_d == nullptr) return MLA_ERR_INVALID_ARG;
+  return materialized_common(dims, q_nope, q_pe, nullptr, kv_q, kv_d, wk_b, wv_b, n_kv, T, q_pos0, head_chunk,
+                             workspace, ws_bytes, o, lse, stream);
+}
+
+int mla_output_project(const mla_dims* dims, const void* o, const void* w_o, float* u, int32_t T, int32_t D,
+                       void* stream) {
+  int s = check_dims(dims);
+  if (s != MLA_OK) return s;
+  s = check_ptrs({o, w_o, u});
+  if (s != MLA_OK) return s;
+  if (T < 1 || D < 64) return MLA_ERR_INVALID_ARG;
+  if (D % 64 != 0 || D > (1 << 20)) return MLA_ERR_UNSUPPORTED;
+  int* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
+  return to_status(launch_wo_gemm_tc(o, w_o, u, T, dims->n_head * kVHead, D, err, kDefaultWaitUs,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 size_t mla_prefill_workspace_size(const mla_dims* dims, int32_t n_kv) {
@@ -307,6 +399,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
     case MLA_ERR_CUDA: return "CUDA runtime error";
     case MLA_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    case MLA_ERR_RANGE: return "value outside the fp16 range met an fp16 operand";
     default: return "unknown status";
   }
 }

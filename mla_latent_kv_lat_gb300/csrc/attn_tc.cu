@@ -286,16 +286,58 @@ struct ItemIter<true> {
   int c, g;
   int b;                       // next sequence
   int64_t lo, hi, S;           // cluster tile range, first tile of sequence b
+  // Tiles of sequences [q0, q0 + 8) (invalid ones count 0), and with `stop`
+  // the number of them that end at or before tile `stop` given the run
+  // reaches `base` at q0.  The loads of all eight are in flight at once: the
+  // sequence table is read by every role of every CTA at the start.
+  MLA_DEVINL void batch(int q0, int32_t (&tiles)[8]) const {
+    int32_t len[8];
+    int64_t st[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool in = q0 + j < a->n_seq;
+      len[j] = in ? a->seq_len[q0 + j] : 0;
+      st[j] = in ? a->seq_start[q0 + j] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool ok = len[j] >= 1 && len[j] <= a->max_len && st[j] >= 0 && st[j] <= a->n_rows - len[j];
+      tiles[j] = ok ? static_cast<int32_t>(decode_seq_tiles(len[j])) : 0;     // invalid: skipped
+    }
+  }
   MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
-    a = &args; c = cluster; g = clusters; b = 0; S = 0;
+    a = &args; c = cluster; g = clusters;
     int64_t T = 0;
-    for (int q = 0; q < a->n_seq; ++q) T += decode_seq_tiles(a->seq_len[q]);
+    for (int q0 = 0; q0 < a->n_seq; q0 += 8) {
+      int32_t t[8];
+      batch(q0, t);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) T += t[j];
+    }
     lo = decode_cluster_lo(T, g, c);
     hi = decode_cluster_lo(T, g, c + 1);
+    // skip the sequences that end before this cluster's range
+    b = 0;
+    S = 0;
+    for (int q0 = 0; q0 < a->n_seq; q0 += 8) {
+      int32_t t[8];
+      batch(q0, t);
+      bool stop = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (!stop && S + t[j] <= lo && q0 + j < a->n_seq) {
+          S += t[j];
+          b = q0 + j + 1;
+        } else {
+          stop = true;
+        }
+      }
+      if (stop) break;
+    }
   }
   MLA_DEVINL bool next(Item& it) {
     while (b < a->n_seq && S < hi) {
-      const int32_t len = a->seq_len[b];
+      const int32_t len = decode_valid_len(a->seq_start, a->seq_len, b, a->max_len, a->n_rows);   // 0: skipped
       const int64_t tb = decode_seq_tiles(len);
       const int64_t p_lo = max(lo, S), p_hi = min(hi, S + tb);
       const int bb = b;
@@ -341,7 +383,10 @@ struct TileCursor {
 
 // bf16 -> fp16 in place of this thread's share (thread ct of kConvThreads) of
 // a landed latent tile.  A 16-byte unit holds 8 consecutive values of one key,
-// so the swizzle does not matter; exact over fp16's normal range.
+// so the swizzle does not matter; exact over fp16's normal range.  (A value
+// too large for fp16 becomes inf here; every key of a tile goes through P.V,
+// so it makes the piece's output infinite or NaN, which the epilogue checks:
+// a check per value here would lengthen the tile's conversion step.)
 MLA_DEVINL void convert_share(uint8_t* stage, int ct) {
   constexpr int kUnits = kLatStage / 16;
   constexpr int kPer = (kUnits + kConvThreads - 1) / kConvThreads;
@@ -422,6 +467,7 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
     ahead.next();
   }
   P x, y;
+  uint32_t dmax = 0;                          // largest |scale| bit pattern (fp16 range check)
   int64_t cur_row = cur.it.key_base + static_cast<int64_t>(cur.t) * kBK;
   x.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
   cur.next();
@@ -450,6 +496,10 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
       }
     }
     now.store(sLat + ls * kLatStage, sRope + rs * kChunk, pt);
+    if constexpr (kQ8) {
+#pragma unroll
+      for (int t = 0; t < P::NU; ++t) dmax = max(dmax, now.d[t] & 0x7FFFu);
+    }
     tc::fence_proxy_async();
     mbar_arrive(&B.lat_full[ls]);
     cur_row = nxt_row;
@@ -460,9 +510,10 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   // instruction-cache misses of a second copy of the step.
 #pragma unroll 1
   for (int u = 0;; ++u) {
-    if (!step(u, x, y)) return;
+    if (!step(u, x, y)) break;
     x = y;
   }
+  if (kQ8 && f16_scale_overflows(dmax)) record_error(a.err, MLA_ERR_RANGE);
 }
 
 // ---------------------------------------------------------------------------
@@ -610,6 +661,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     };
 
     uint32_t own[kKpt / 2], nxt[kKpt / 2];
+    uint32_t qrun = 0;                          // q_pe converted here (q8_0 decode): fp16 range check
+    bool score_range = false;                   // a row maximum became infinite or NaN
     int u0 = 0;                                 // this item's first tile, counted across items
     int k = 0;                                  // items done
     ItemIter<kDecode> items;
@@ -652,7 +705,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         tc::tmem_st_wait();
         if (rank == 0) {                        // RoPE query part -> smem (bf16 as is, or fp16)
 #pragma unroll
-          for (int v = 0; v < 8 / kTpr; ++v) st_unit(sQr, i, (8 / kTpr) * hh + v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+          for (int v = 0; v < 8 / kTpr; ++v) {
+            if (kRopeF16) {
+              qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].x), qpe[v].y);
+              qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].z), qpe[v].w);
+            }
+            st_unit(sQr, i, (8 / kTpr) * hh + v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+          }
           tc::fence_proxy_async();
         }
         tc::fence_before_sync();
@@ -794,6 +853,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         }
       }
       // ---- end of item -----------------------------------------------------------
+      // A partial score past fp16's range makes the row maximum infinite (or NaN).
+      if (rvalid && !dead && !(m_run < INFINITY)) score_range = true;
       if constexpr (kEpi) {
         // Prefill: hand the row sums to the epilogue warps and go on.
         group_meet(aux_l, l_h, u0 + n);
@@ -847,6 +908,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       u0 += n;
       ++k;
     }
+    if (score_range || bf16x2_absmax_overflows(qrun)) record_error(a.err, MLA_ERR_RANGE);
   } else if (kEpi && (warp < kLoaderWarp || (kDecode && !kQ8 && warp > kLoaderWarp && warp < kMmaWarp))) {
     if constexpr (!kDecode) {
     // ======================= Q loading and epilogue (prefill) ==================
@@ -889,6 +951,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     };
     Item prev;
     int k = 0;
+    uint32_t qrun = 0;                          // q_pe values converted to fp16: range check
 #pragma unroll 1
     for (int rnd = 0; ok && rnd * stride < a.n_items; ++rnd) {
       const int idx = round_item(first, stride, rnd);
@@ -922,7 +985,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 #pragma unroll
         for (int v = 0; v < 8; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) st_unit(sQr, i, v, bf16x8_to_f16x8(qpe[v]));
+        for (int v = 0; v < 8; ++v) {
+          qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].x), qpe[v].y);
+          qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].z), qpe[v].w);
+          st_unit(sQr, i, v, bf16x8_to_f16x8(qpe[v]));
+        }
         tc::fence_proxy_async();
       }
       tc::fence_before_sync();
@@ -945,6 +1012,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       ++k;
     }
     if (ok && k > 0) epilogue(prev, k - 1);
+    if (bf16x2_absmax_overflows(qrun)) record_error(a.err, MLA_ERR_RANGE);
     } else {
     // ============ Q loading, tile conversion and epilogue (bf16 decode) ========
     // As for prefill, per item (piece): Q once the previous item's last score
@@ -959,6 +1027,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     const int q4 = warp & 3;
     const int i = q4 * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    float amax = 0.f;                           // |O| of the partials (fp16 range check)
     bool ok = true;
     auto epilogue = [&](const Item& pv, int kk) {
       ok = ok && wait_all(&B.o_ready, kk & 1, a);
@@ -975,6 +1044,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         uint32_t o[32];
         tc::tmem_ld32(tmem + lanes + kTmO + 32 * c, o);
         tc::tmem_ld_wait();
+        if (i < pv.nvalid) {                    // a cache value past fp16 made O infinite or NaN
+#pragma unroll
+          for (int e = 0; e < 32; ++e) amax = f32_absmax(amax, __uint_as_float(o[e]));
+        }
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint4 w[4];
@@ -1073,6 +1146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
           ++k;
         }
       }
+      if (!(amax < INFINITY)) record_error(a.err, MLA_ERR_RANGE);   // O = l x o_lat may pass 65504: finiteness only
     }
     }
   } else if (warp < kMmaWarp) {

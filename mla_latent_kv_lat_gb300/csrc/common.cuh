@@ -81,6 +81,29 @@ MLA_DEVINL void i8x4_to_f16x4(uint32_t w, uint32_t d2, uint32_t& lo, uint32_t& h
   hi = *reinterpret_cast<const uint32_t*>(&r1);
 }
 
+// fp16 range checks.  A thread keeps a running maximum and records
+// MLA_ERR_RANGE once, at the end of its work, if the maximum says a value fp16
+// cannot hold went by.
+//   bf16 words: the maximum of |x| bit patterns in each 16-bit half.  bf16 has
+//   no value between 65504 (fp16's largest) and 65536 = 0x4780, so a half at or
+//   above 0x4780 is too large for fp16, or an infinity or a NaN (0x7F80 and up).
+MLA_DEVINL uint32_t bf16x2_absmax(uint32_t run, uint32_t w) { return __vmaxu2(run, w & 0x7FFF7FFFu); }
+MLA_DEVINL bool bf16x2_absmax_overflows(uint32_t run) {
+  return (run & 0xFFFFu) >= 0x4780u || (run >> 16) >= 0x4780u;
+}
+//   q8_0 block scales (fp16 bits): |d| >= 516 lets 127 x d pass 65504 (the
+//   largest code of a block from the quantiser is +-127); 0x6008 = 516.
+MLA_DEVINL bool f16_scale_overflows(uint32_t run_abs_bits) { return run_abs_bits >= 0x6008u; }
+//   fp32 values about to be rounded to fp16: fp16(x) is infinite for
+//   |x| >= 65520.  The running maximum keeps a NaN (max.NaN), and the negated
+//   comparison flags it.
+MLA_DEVINL float f32_absmax(float run, float x) {
+  float r;
+  asm("{\n\t.reg .f32 t;\n\tabs.f32 t, %2;\n\tmax.NaN.f32 %0, %1, t;\n\t}" : "=f"(r) : "f"(run), "f"(x));
+  return r;
+}
+MLA_DEVINL bool f32_overflows_f16(float run_absmax) { return !(run_absmax < 65520.f); }
+
 MLA_DEVINL float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

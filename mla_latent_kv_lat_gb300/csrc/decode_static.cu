@@ -28,7 +28,9 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so its device address is looked
-// up once per device, with that device current, and cached.
+// up once per device, with that device current, and cached for the life of
+// the process (after a cudaDeviceReset of that device the cached address is
+// stale: the header tells callers not to use the library on it again).
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
@@ -49,7 +51,10 @@ extern "C" int mla_attn_decode_static(const mla_dims* dims, const void* q_lat, c
                                       int64_t n_rows, const int64_t* seq_start, const int32_t* seq_len, int32_t B,
                                       int32_t max_len, void* o_lat, void* stream) {
   const size_t need = mla_decode_workspace_size(dims, B, max_len);
-  if (need == 0) return MLA_ERR_INVALID_ARG;
+  // Arguments no workspace can serve: mla_attn_decode's own checks give the
+  // status (they run before its workspace check, so nothing is launched).
+  if (need == 0)
+    return mla_attn_decode(dims, q_lat, q_pe, kv, n_rows, seq_start, seq_len, B, max_len, nullptr, 0, o_lat, stream);
   if (need > kStaticScratchBytes) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int s = scratch_for_current_device(&scratch);

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
   __shared__ long long red[2][kCombHeads];
   long long tb = 0, tt = 0;
   for (int q = threadIdx.x; q < c.B; q += blockDim.x) {
-    const long long t = decode_seq_tiles(c.seq_len[q]);
+    const long long t = decode_seq_tiles(decode_valid_len(c.seq_start, c.seq_len, q, c.max_len, c.n_rows));
     tt += t;
     if (q < b) tb += t;
   }
@@ -95,7 +95,12 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
     Sb += red[0][w];
     T += red[1][w];
   }
-  const int64_t Eb = Sb + decode_seq_tiles(c.seq_len[b]);
+  const int32_t len_b = decode_valid_len(c.seq_start, c.seq_len, b, c.max_len, c.n_rows);
+  if (len_b == 0) {                  // an invalid request: skipped by the attention kernel too
+    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(c.err, MLA_ERR_INVALID_ARG);
+    return;
+  }
+  const int64_t Eb = Sb + decode_seq_tiles(len_b);
   const int G = c.n_clusters;
   // The first cluster whose range meets [Sb, Eb): ranges are [lo(c), lo(c+1)).
   int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Sb * G / max(T, static_cast<int64_t>(1))));
@@ -191,10 +196,14 @@ cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream) {
 // q8_0 codes become fp16(scale x code), the value the decode kernel forms.
 // ---------------------------------------------------------------------------
 namespace {
-__global__ void __launch_bounds__(256) cache_bf16_to_f16_kernel(const uint4* kv, uint4* out, int64_t n_units) {
+__global__ void __launch_bounds__(256) cache_bf16_to_f16_kernel(const uint4* kv, uint4* out, int64_t n_units,
+                                                                 int* err) {
+  uint32_t run = 0;                  // |x| bit patterns seen (fp16 range check)
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n_units;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 v = __ldg(kv + u);
+    run = bf16x2_absmax(bf16x2_absmax(run, v.x), v.y);
+    run = bf16x2_absmax(bf16x2_absmax(run, v.z), v.w);
     uint4 o;
     float2 f;
     f = bf16x2_to_f32(v.x); o.x = pack_f16x2(f.x, f.y);
@@ -203,18 +212,21 @@ __global__ void __launch_bounds__(256) cache_bf16_to_f16_kernel(const uint4* kv,
     f = bf16x2_to_f32(v.w); o.w = pack_f16x2(f.x, f.y);
     out[u] = o;
   }
+  if (bf16x2_absmax_overflows(run)) record_error(err, MLA_ERR_RANGE);
 }
 
 // One thread per 16 codes (half a q8_0 block): 36 per row.
 __global__ void __launch_bounds__(256) cache_q8_0_to_f16_kernel(const int8_t* kv_q, const __half* kv_d, int64_t ld_d,
-                                                                 uint4* out, int64_t rows) {
+                                                                 uint4* out, int64_t rows, int* err) {
   const int64_t n_units = rows * (kRow / 16);
+  uint32_t dmax = 0;                 // largest |scale| bit pattern seen (fp16 range check)
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < n_units;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = u / (kRow / 16);
     const int c = static_cast<int>(u % (kRow / 16));
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(kv_q + row * kRow) + c);
     const uint32_t ds = __half_as_ushort(__ldg(kv_d + static_cast<int64_t>(c >> 1) * ld_d + row));
+    dmax = max(dmax, ds & 0x7FFFu);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t h[8];
 #pragma unroll
@@ -222,6 +234,7 @@ __global__ void __launch_bounds__(256) cache_q8_0_to_f16_kernel(const int8_t* kv
     out[2 * u] = make_uint4(h[0], h[1], h[2], h[3]);
     out[2 * u + 1] = make_uint4(h[4], h[5], h[6], h[7]);
   }
+  if (f16_scale_overflows(dmax)) record_error(err, MLA_ERR_RANGE);
 }
 
 unsigned stage_blocks(int64_t n_units) {
@@ -231,15 +244,15 @@ unsigned stage_blocks(int64_t n_units) {
 }  // namespace
 
 cudaError_t launch_stage_cache_f16(const void* kv, const int8_t* kv_q, const uint16_t* kv_d, int64_t ld_d,
-                                   int64_t rows, void* out, cudaStream_t stream) {
+                                   int64_t rows, void* out, int* err, cudaStream_t stream) {
   if (kv != nullptr) {
     const int64_t n_units = rows * (kRow / 8);
     cache_bf16_to_f16_kernel<<<stage_blocks(n_units), 256, 0, stream>>>(static_cast<const uint4*>(kv),
-                                                                         static_cast<uint4*>(out), n_units);
+                                                                         static_cast<uint4*>(out), n_units, err);
   } else {
     const int64_t n_units = rows * (kRow / 16);
     cache_q8_0_to_f16_kernel<<<stage_blocks(n_units), 256, 0, stream>>>(
-        kv_q, reinterpret_cast<const __half*>(kv_d), ld_d, static_cast<uint4*>(out), rows);
+        kv_q, reinterpret_cast<const __half*>(kv_d), ld_d, static_cast<uint4*>(out), rows, err);
   }
   return cudaGetLastError();
 }

@@ -14,7 +14,10 @@ key_length 576 = 512 latent + 64 rope, value_length 512, nope 128, v 128):
 * ``k_pe``  [n_rows, 64]   RoPE keys, shared by every head,
 * ``q_nope``[T, H, 128], ``q_pe`` [T, H, 64] queries (RoPE already applied),
 * ``wk_b``  [H, 128, 512]  K up-projection (per head),
-* ``wv_b``  [H, 512, 128]  V up-projection (per head).
+* ``wv_b``  [H, 512, 128]  V up-projection (per head),
+* ``w_o``   [H, 128, D]    the output projection after the path (``make_wo``;
+  D = 2048 for the Lite shape, 7168 for the V3 shape -- the two models' hidden
+  sizes, which the pages do not print).
 
 Distributions: activations N(0, 1); weights N(0, std = 1/sqrt(fan_in)) with
 fan_in = 128 for wk_b and 512 for wv_b.  Every value is drawn in fp32 from one
@@ -75,6 +78,7 @@ class Workload:
     B: int = 0                # decode: sequences
     len_lo: int = 0           # decode: cache length range, inclusive
     len_hi: int = 0
+    hidden: int = 0           # model width D of the output projection wo [H*128, D]
     describe: str = ""
 
     @property
@@ -84,25 +88,25 @@ class Workload:
 
 WORKLOADS = {
     "lite_t256": Workload(
-        "lite_t256", "prefill", 16, "bf16", T=256, q_pos0=0, n_kv=256,
+        "lite_t256", "prefill", 16, "bf16", T=256, q_pos0=0, n_kv=256, hidden=2048,
         describe="DeepSeek-Lite shape, 16 heads, 256-token causal prefill over its own 256-row cache"),
     "lite_t4096": Workload(
-        "lite_t4096", "prefill", 16, "bf16", T=4096, q_pos0=0, n_kv=4096,
+        "lite_t4096", "prefill", 16, "bf16", T=4096, q_pos0=0, n_kv=4096, hidden=2048,
         describe="DeepSeek-Lite shape, 16 heads, 4096-token causal prefill"),
     "v3_chunk8192_at32768": Workload(
-        "v3_chunk8192_at32768", "prefill", 128, "bf16", T=8192, q_pos0=32768, n_kv=40960,
+        "v3_chunk8192_at32768", "prefill", 128, "bf16", T=8192, q_pos0=32768, n_kv=40960, hidden=7168,
         describe="DeepSeek-V3 shape, 128 heads, 8192-query chunked prefill at positions "
                  "32768..40959 over a 40960-row latent cache"),
     "v3_decode_b32": Workload(
-        "v3_decode_b32", "decode", 128, "bf16", B=32, len_lo=4096, len_hi=32768,
+        "v3_decode_b32", "decode", 128, "bf16", B=32, len_lo=4096, len_hi=32768, hidden=7168,
         describe="DeepSeek-V3 shape decode, 32 sequences, one query each, "
                  "cache lengths uniform in [4096, 32768]"),
     "v3_q8_chunk8192_at90112": Workload(
-        "v3_q8_chunk8192_at90112", "prefill", 128, "q8_0", T=8192, q_pos0=90112, n_kv=98304,
+        "v3_q8_chunk8192_at90112", "prefill", 128, "q8_0", T=8192, q_pos0=90112, n_kv=98304, hidden=7168,
         describe="DeepSeek-V3 shape, q8_0 latent cache, 8192-query causal prefill at "
                  "positions 90112..98303 over 98304 rows"),
     "v3_q8_decode_b8": Workload(
-        "v3_q8_decode_b8", "decode", 128, "q8_0", B=8, len_lo=98304, len_hi=98304,
+        "v3_q8_decode_b8", "decode", 128, "q8_0", B=8, len_lo=98304, len_hi=98304, hidden=7168,
         describe="DeepSeek-V3 shape, q8_0 latent cache, 8 sequences decoding at length 98304"),
     # The step before the path: T new tokens' rows (RoPE applied) into a bf16
     # and a q8_0 cache of n_kv rows, at distinct random slots -- the fill of
@@ -207,6 +211,14 @@ def make_inputs(wl: Workload | str, seed: int = 0, *, n_head: Optional[int] = No
     wk_b = normal_bf16(rng, (H, QK_NOPE, KV_LORA_RANK), 1.0 / math.sqrt(QK_NOPE))
     wv_b = normal_bf16(rng, (H, KV_LORA_RANK, V_HEAD), 1.0 / math.sqrt(KV_LORA_RANK))
     return Inputs(wl, c_kv, k_pe, q_nope, q_pe, wk_b, wv_b, seq_len, seq_start)
+
+
+def make_wo(n_head: int, hidden: int, seed: int = 0) -> np.ndarray:
+    """The output projection wo as [H, 128, hidden] (row-major [H*128, hidden]):
+    N(0, std = 1/sqrt(H*128)) rounded to bf16, from its own generator (seeded
+    with (seed, 1)), so that drawing it changes none of the other inputs."""
+    rng = np.random.default_rng([seed, 1])
+    return normal_bf16(rng, (n_head, V_HEAD, hidden), 1.0 / math.sqrt(n_head * V_HEAD))
 
 
 def sample_rows(n: int, k: int, seed: int = 0, must: tuple = ()) -> np.ndarray:

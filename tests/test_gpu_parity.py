@@ -114,7 +114,11 @@ def test_prefill_latent_attention_matches_oracle(H, T, q_pos0, n_kv):
                 + np.einsum("thr,jr->thj", x.q_pe.astype(np.float64), x.k_pe))
     s1 = np.abs(np.einsum("thc,jc->thj", q_lat[..., half:].astype(np.float64), x.c_kv[:, half:]))
     bound = 2.0 ** -11 * (s0 + s1).max() * x.wl.scale + 2.0 ** -11 * 8 * np.log(2) + 1e-5
-    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= bound
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got_lse - ref_lse)) <= bound
+    # and, independently of that kernel-derived bound, the normaliser exp(lse)
+    # itself within the stated 1e-2 relative level of the oracle's
+    assert np.max(np.abs(np.expm1(got_lse - ref_lse))) <= 1e-2
     _check_no_device_error()
 
 
@@ -320,7 +324,10 @@ def _caches(n_rows, ld_d):
     return kv, kv_q, kv_d
 
 
-@pytest.mark.parametrize("n,n_rows", [(1, 4), (333, 1000), (4096, 98304)])
+# 40001 tokens: more than one pass of the kernel's grid-stride loop over groups
+# of four tokens (one pass covers 4 tokens x 8 warps x 8 blocks per SM), and
+# not a multiple of four.
+@pytest.mark.parametrize("n,n_rows", [(1, 4), (333, 1000), (4096, 98304), (40001, 98304)])
 def test_rope_append_matches_oracle(n, n_rows):
     a = W.make_append_inputs(n, n_rows, seed=n)
     c, k, pos, slot = _append_dev(a)
@@ -331,11 +338,14 @@ def test_rope_append_matches_oracle(n, n_rows):
     got = kv.view(torch.int16).cpu().numpy().view(np.uint16)
     ref = W.to_bf16(O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS).astype(np.float32))[1]
     rows = got[a.slot]
-    # The latent part is copied: bit-exact.  The RoPE part: the device rotates
-    # in fp32 (angle reduced in fp64) and rounds once to bf16, so it is within
-    # half a bf16 step (2^-8 relative) of the exact rotation, plus the fp32
-    # error of ~1e-6 of the pair's magnitude (which matters only where the
-    # two terms cancel).
+    # The latent part is copied: bit-exact.  The RoPE part: the device takes
+    # the angle as an exact 0.64 fixed-point fraction of a turn (pos x frac(t_i)
+    # modulo one turn), feeds its top 32 bits to sincospif (angle error
+    # < 2^-23 rad from the truncation, plus sincospif's own few-ulp fp32 error),
+    # rotates in fp32 and rounds once to bf16.  So the result is within half a
+    # bf16 step (2^-8 relative) of the exact rotation, plus ~1e-6 of the pair's
+    # magnitude from the fp32 sine, cosine and products (which matters only
+    # where the two terms cancel).
     assert np.array_equal(rows[:, :512], ref[:, :512])
     exact = O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS)[:, 512:]
     pair = np.repeat(np.maximum(np.abs(a.k_pe[:, 0::2]), np.abs(a.k_pe[:, 1::2])), 2, axis=1).astype(np.float64)
@@ -383,15 +393,35 @@ def test_rope_append_then_decode_reads_the_rows():
     assert_tol(bufs.o.cpu().numpy(), ref, TOL_BF16, "decode o on appended rows")
 
 
-def test_rope_append_out_of_range_slot_is_skipped_and_reported():
+@pytest.mark.parametrize("bad", ["slot", "pos"])
+def test_rope_append_out_of_range_slot_is_skipped_and_reported(bad):
+    # token 3 is bad (slot one past the end, or a negative position); tokens
+    # 0..2 share its group of four tokens in the kernel's RoPE pass, so their
+    # RoPE columns and q8_0 rows are where a masking mistake would show
     a = W.make_append_inputs(8, 16, seed=3)
-    a.slot[3] = 16                              # one past the end
+    if bad == "slot":
+        a.slot[3] = 16
+    else:
+        a.pos[3] = -5
     c, k, pos, slot = _append_dev(a)
     kv, kv_q, kv_d = _caches(16, 16)
-    mla.mla_rope_append(c, k, pos, slot, kv=kv, kv_q=kv_q, kv_d=kv_d)
+    mla.mla_rope_append(c, k, pos, slot, kv=kv, kv_q=kv_q, kv_d=kv_d, freq_base=FB, freq_scale=FS)
     assert mla.mla_get_device_error() == -1     # MLA_ERR_INVALID_ARG, read and cleared
     got = kv.view(torch.int16).cpu().numpy().view(np.uint16)
-    ref = W.to_bf16(O.cache_rows(a.c_kv, a.k_pe, a.pos, FB, FS).astype(np.float32))[1]
     ok = [j for j in range(8) if j != 3]
-    assert np.array_equal(got[a.slot[ok], :512], ref[ok, :512])
+    exact = O.cache_rows(a.c_kv[ok], a.k_pe[ok], a.pos[ok], FB, FS)
+    ref = W.to_bf16(exact.astype(np.float32))[1]
+    rows = got[a.slot[ok]]
+    assert np.array_equal(rows[:, :512], ref[:, :512])
+    pair = np.repeat(np.maximum(np.abs(a.k_pe[ok, 0::2]), np.abs(a.k_pe[ok, 1::2])), 2, axis=1).astype(np.float64)
+    err = np.abs(W.bf16_bits_to_f32(rows[:, 512:]).astype(np.float64) - exact[:, 512:])
+    assert (err <= 2.0 ** -8 * np.abs(exact[:, 512:]) + 1e-6 * pair).all()
+    codes, scales = O.quantize_q8_0(W.bf16_bits_to_f32(rows))
+    assert np.array_equal(kv_q.cpu().numpy()[a.slot[ok]], codes)
+    assert np.array_equal(kv_d.cpu().numpy()[:, a.slot[ok]].T.view(np.uint16), scales.view(np.uint16))
+    # every other row, the bad token's neighbours in the cache included, is untouched
+    untouched = np.setdiff1d(np.arange(16), a.slot[ok])
+    assert not got[untouched].any()
+    assert not kv_q.cpu().numpy()[untouched].any()
+    assert not kv_d.cpu().numpy()[:, untouched].view(np.uint16).any()
     assert mla.mla_get_device_error() == 0
