@@ -495,6 +495,12 @@ def run_ours(args, torch, dist, rank, world):
     pk, pk_kind = peaks()
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
 
+    if ":" in args.workload:              # a materialised or projected prefill as the headline
+        out = measure_variant(args, torch, args.workload, flush, pk, pk_kind, world)
+        out.update({"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                    "data": "synthetic", "config": {"workload": args.workload}})
+        return out
     # the headline workload: clocks sampled during its timed steps
     wl, x, d, bufs, step, launches = setup_workload(args.workload, torch)
     if dist is not None:
@@ -834,7 +840,12 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="headline workload: one of " + ", ".join(sorted(W.WORKLOADS)) +
+                         " (a prefill may take :materialized or :projected)")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="prefill: time the last CHUNK queries of the workload instead of all of them (same "
+                         "shape and positions; for small profiling cases)")
     ap.add_argument("--secondary", default="all",
                     help="workloads measured after the headline one: all (default), none, or a comma list")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -845,6 +856,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    base, _, variant = args.workload.partition(":")
+    if base not in W.WORKLOADS or variant not in ("", "materialized", "projected"):
+        raise SystemExit(f"unknown workload {args.workload}")
+    if args.chunk:
+        wl = W.WORKLOADS[base]
+        if wl.kind != "prefill" or not 0 < args.chunk <= wl.T:
+            raise SystemExit("--chunk applies to prefill workloads, 0 < CHUNK <= T")
+        # the last CHUNK queries: positions q_pos0 + T - CHUNK .., over the same cache
+        import dataclasses
+        W.WORKLOADS[base] = dataclasses.replace(wl, name=f"{base}_last{args.chunk}", T=args.chunk,
+                                                q_pos0=wl.q_pos0 + wl.T - args.chunk)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -51,9 +51,11 @@
  * - Kernels that wait on asynchronous copies or tensor-core work bound every
  *   wait (0.5 s of the GPU's global timer).  A wait that runs out records
  *   MLA_ERR_TIMEOUT in a per-device error word, abandons its tile and
- *   returns; mla_get_device_error() reads and clears it.  While the word is
- *   set, any wait that does not complete at once gives up too, so a failing
- *   launch (and any launch after it, until the word is read) ends quickly.
+ *   returns; mla_get_device_error() reads and clears it.  While the word
+ *   holds a timeout, any wait that does not complete at once gives up too, so
+ *   a failing launch (and any launch after it, until the word is read) ends
+ *   quickly.  The other device-side errors (MLA_ERR_RANGE, a skipped
+ *   request) only record themselves: later launches run as usual.
  * - Dims other than kv_lora_rank 512, qk_rope 64, qk_nope 128, v_head 128,
  *   or n_head not a multiple of 16 in [16, 128], return MLA_ERR_UNSUPPORTED.
  *

@@ -192,17 +192,21 @@ MLA_DEVINL uint64_t global_timer_ns() {
 
 // The slow path shared by the bounded waits: keep trying (suspended between
 // tries) until `done()` holds, `limit_us` microseconds have passed (records
-// MLA_ERR_TIMEOUT) or another thread has already recorded an error, in which
+// MLA_ERR_TIMEOUT) or another thread has already recorded a timeout, in which
 // case the launch is failing anyway and this wait gives up at once, so that a
 // failed launch ends quickly instead of each CTA timing out in turn.  While
-// the error word is set (until the host reads it), a wait that does not
-// complete at once gives up.
+// the error word holds a timeout (until the host reads it), a wait that does
+// not complete at once gives up.  Other recorded errors (a value out of fp16
+// range, a skipped request) leave the waits alone.
+MLA_DEVINL bool timeout_recorded(const int* err) {
+  return err != nullptr && *reinterpret_cast<const volatile int*>(err) == MLA_ERR_TIMEOUT;
+}
 template <typename Done>
 MLA_DEVINL bool wait_slow(Done done, uint32_t limit_us, int* err) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (done()) return true;
-    if (err != nullptr && *reinterpret_cast<volatile int*>(err) != 0) return false;
+    if (timeout_recorded(err)) return false;
     if (global_timer_ns() - t0 > static_cast<uint64_t>(limit_us) * 1000u) {
       record_error(err, MLA_ERR_TIMEOUT);
       return false;
