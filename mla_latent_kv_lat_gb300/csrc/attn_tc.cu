@@ -10,7 +10,7 @@
 //   * The 512-wide fp32 output of 128 rows would fill all of a CTA's tensor
 //     memory, leaving no room for scores, so the pair splits the latent
 //     dimension: CTA r owns latent columns [256r, 256r+256) of the output and
-//     of the score contraction; CTA 0 also owns the 64 RoPE dimensions.
+//     of the score contraction, and RoPE dimensions [32r, 32r+32).
 //   * Each CTA computes its partial scores on tcgen05 into TMEM: the latent
 //     part as fp16 x fp16 with Q from TMEM, the RoPE part as bf16 x bf16 (the
 //     bf16 cache and q_pe enter it unrounded; with a q8_0 cache both are fp16)
@@ -21,8 +21,9 @@
 //   * Score MMAs run three tiles ahead of the P.V MMAs: the softmax sends tile
 //     j+1's partial before it processes tile j, so the exchange latency and
 //     the score MMAs overlap the softmax.
-//   * P (fp16) goes to shared memory; O_r += P V_r runs on tcgen05 with V_r read
-//     in place from the latent cache tile (MN-major view).
+//   * P (fp16) goes to one of two shared-memory buffers (so P of tile j+1 may
+//     be written while P.V of tile j runs); O_r += P V_r runs on tcgen05 with
+//     V_r read in place from the latent cache tile (MN-major view).
 //   * Cache tiles.  Prefill: every cluster reads every visible cache row, so
 //     the rows are staged once as fp16 (latent and RoPE parts) before the
 //     kernel, and one thread brings each tile in by TMA, already in the
@@ -49,13 +50,19 @@ constexpr int kChunk = kBK * 128;            // 8 KB: 64 keys x 64 16-bit values
 constexpr int kLatStage = 4 * kChunk;        // 32 KB: this CTA's 256 latent dims
 constexpr int kLatStages = 4;
 constexpr int kRopeStages = 2;   // a RoPE tile is done with long before its latent stage
-constexpr int kQRopeBytes = kRows * 128;     // 16 KB: 128 rows x 64 dims
-constexpr int kPBytes = kRows * 128;         // 16 KB: 128 rows x 64 keys fp16
+// The 64 RoPE dims are split between the CTAs too: CTA r owns dims [32r, 32r+32)
+// of the query and key RoPE parts (64-byte rows, 64-byte swizzle), so each CTA
+// holds half a RoPE query tile and half a RoPE key ring; the 16 KB this frees
+// pays for the second P buffer.
+constexpr int kRopeHalf = 32;
+constexpr int kRopeChunk = kBK * kRopeHalf * 2;   // 4 KB: 64 keys x 32 dims
+constexpr int kQRopeBytes = kRows * kRopeHalf * 2;   // 8 KB: 128 rows x 32 dims
+constexpr int kPBytes = kRows * 128;         // 16 KB: 128 rows x 64 keys fp16 (two buffers)
 constexpr int kXBytes = kRows * kBK * 2;     // 16 KB: one exchange buffer (fp16 partial scores)
 constexpr int kOffLat = kQRopeBytes;
 constexpr int kOffRope = kOffLat + kLatStages * kLatStage;
-constexpr int kOffP = kOffRope + kRopeStages * kChunk;
-constexpr int kOffX = kOffP + kPBytes;
+constexpr int kOffP = kOffRope + kRopeStages * kRopeChunk;
+constexpr int kOffX = kOffP + 2 * kPBytes;
 constexpr int kOffAux = kOffX + 2 * kXBytes;
 // Two softmax threads per query row, each taking 32 keys of every tile (the
 // code is written for kTpr threads per row; one and four measured slower).
@@ -128,7 +135,7 @@ struct Bars {
   uint64_t x_full[2];
   uint64_t x_empty[2];
   uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t pv_done[2];   // by P buffer: P.V of the tile that used it has completed
   uint64_t q_ready;   // arrival per item: Q of the next item is in TMEM
   uint64_t o_free;    // arrival per item: the epilogue has read O
   uint64_t q_free;    // commit per item (prefill): its last score MMA has completed
@@ -148,6 +155,11 @@ MLA_DEVINL void st_unit(uint8_t* base, int row, int u, uint4 v) {
   *reinterpret_cast<uint4*>(base + row * 128 + ((u ^ (row & 7)) << 4)) = v;
 }
 
+// The same for a 64-byte-swizzled tile (rows of 32 halves): unit u in [0, 4).
+MLA_DEVINL void st_unit64(uint8_t* base, int row, int u, uint4 v) {
+  *reinterpret_cast<uint4*>(base + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) = v;
+}
+
 MLA_DEVINL uint4 bf16x8_to_f16x8(uint4 v) {
   uint4 o;
   float2 f;
@@ -162,14 +174,14 @@ MLA_DEVINL uint4 bf16x8_to_f16x8(uint4 v) {
 // ---------------------------------------------------------------------------
 // Producer: one 64-key tile of this CTA's cache part.
 //   bf16 cache: the 256 latent dims (32 units of 8 values per key); the RoPE
-//               part of rank 0 comes by TMA.
-//   q8_0 cache: the 256 latent dims (16 units of 16 codes per key) plus, on
-//               rank 0, the 64 RoPE dims (4 units), dequantised to fp16.
+//               part comes by TMA.
+//   q8_0 cache: the 256 latent dims (16 units of 16 codes per key) plus this
+//               CTA's 32 RoPE dims (2 units), dequantised to fp16.
 // ---------------------------------------------------------------------------
 template <bool kQ8, bool kRope>
 struct Producer {
   static constexpr int LAT_UPK = kQ8 ? 16 : 32;
-  static constexpr int UPK = LAT_UPK + ((kQ8 && kRope) ? 4 : 0);
+  static constexpr int UPK = LAT_UPK + ((kQ8 && kRope) ? 2 : 0);
   static constexpr int NUNITS = kBK * UPK;
   static constexpr int NU = (NUNITS + kProducerThreads - 1) / kProducerThreads;
   uint4 v[NU];
@@ -189,7 +201,7 @@ struct Producer {
           v[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.kv) + row * kRow + 256 * rank +
                                                       cu * 8));
         } else {
-          const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + (cu - 16) * 16;
+          const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + kRopeHalf * rank + (cu - 16) * 16;
           v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
           d[t] = __ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row);
         }
@@ -206,7 +218,6 @@ struct Producer {
       if constexpr (!kQ8) {
         st_unit(lat + (cu >> 3) * kChunk, key, cu & 7, bf16x8_to_f16x8(v[t]));
       } else {
-        uint8_t* base = cu < 16 ? lat + (cu >> 2) * kChunk : rope;
         const int u = (cu & 3) * 2;
         uint4 lo, hi;
         const uint32_t d2 = d[t] | (d[t] << 16);
@@ -214,8 +225,13 @@ struct Producer {
         i8x4_to_f16x4(v[t].y, d2, lo.z, lo.w);
         i8x4_to_f16x4(v[t].z, d2, hi.x, hi.y);
         i8x4_to_f16x4(v[t].w, d2, hi.z, hi.w);
-        st_unit(base, key, u, lo);
-        st_unit(base, key, u + 1, hi);
+        if (cu < 16) {
+          st_unit(lat + (cu >> 2) * kChunk, key, u, lo);
+          st_unit(lat + (cu >> 2) * kChunk, key, u + 1, hi);
+        } else {
+          st_unit64(rope, key, u, lo);
+          st_unit64(rope, key, u + 1, hi);
+        }
       }
     }
   }
@@ -448,8 +464,8 @@ MLA_DEVINL void prefetch_q8_tile(const AttnTcArgs& a, const TileCursor<true>& c,
   }
 }
 
-// kRope: this producer writes the RoPE ring (q8_0 cache, rank 0).  With a bf16
-// cache the RoPE tiles come by TMA, issued when `tma_rope` is set (rank 0).
+// kRope: this producer writes the CTA's RoPE ring (q8_0 cache).  With a bf16
+// cache the RoPE tiles come by TMA, issued when `tma_rope` is set.
 // Tile u counts this cluster's tiles across items.
 template <bool kQ8, bool kRope>
 MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Bars& B, uint8_t* sLat,
@@ -491,11 +507,12 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
       return false;
     if constexpr (!kQ8) {                     // bf16 RoPE keys by TMA, straight into the B-operand layout
       if (tma_rope && pt == 0) {
-        mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
-        tc::tma_load_3d(sRope + rs * kChunk, tm_rope, &B.rope_full[rs], kLatent, static_cast<int>(cur_row), 0);
+        mbar_arrive_expect_tx(&B.rope_full[rs], kRopeChunk);
+        tc::tma_load_3d(sRope + rs * kRopeChunk, tm_rope, &B.rope_full[rs], kLatent + kRopeHalf * rank,
+                        static_cast<int>(cur_row), 0);
       }
     }
-    now.store(sLat + ls * kLatStage, sRope + rs * kChunk, pt);
+    now.store(sLat + ls * kLatStage, sRope + rs * kRopeChunk, pt);
     if constexpr (kQ8) {
 #pragma unroll
       for (int t = 0; t < P::NU; ++t) dmax = max(dmax, now.d[t] & 0x7FFFu);
@@ -522,7 +539,8 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
 // kDecode = false: prefill from the fp16 staging copy (kQ8 unused).
 template <bool kQ8, bool kDecode>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, AttnTcArgs a) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
+                   AttnTcArgs a) {
   // fp16 RoPE operands (prefill staging copy, q8_0 decode) or bf16 (bf16 decode).
   constexpr bool kRopeF16 = kQ8 || !kDecode;
   constexpr int kMmaWarp = mma_warp(kQ8, kDecode);
@@ -572,7 +590,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       mbar_init(&B.x_empty[i], kSoftmaxWarps);
     }
     mbar_init(&B.p_full, kSoftmaxWarps * 32);
-    mbar_init(&B.pv_done, 1);
+    mbar_init(&B.pv_done[0], 1);
+    mbar_init(&B.pv_done[1], 1);
     mbar_init(&B.q_ready, kEpi ? 128 : kSoftmaxWarps * 32);
     mbar_init(&B.o_free, kEpi ? 128 : kSoftmaxWarps * 32);
     mbar_init(&B.q_free, 1);
@@ -688,7 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
                                                           256 * rank + kOpt * hh);
         // All loads first (one round trip), then the stores.
         uint32_t r[kOpt / 64][32];
-        uint4 qpe[8 / kTpr];
+        uint4 qpe[4 / kTpr];
         const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
 #pragma unroll
         for (int c = 0; c < kOpt / 64; ++c)
@@ -698,19 +717,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
             r[c][4 * v] = x.x; r[c][4 * v + 1] = x.y; r[c][4 * v + 2] = x.z; r[c][4 * v + 3] = x.w;
           }
 #pragma unroll
-        for (int v = 0; v < 8 / kTpr; ++v)
-          qpe[v] = rank == 0 && rvalid ? __ldg(qp + (8 / kTpr) * hh + v) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < 4 / kTpr; ++v)      // this CTA's 32 RoPE dims: units 4 rank .. 4 rank + 3
+          qpe[v] = rvalid ? __ldg(qp + 4 * rank + (4 / kTpr) * hh + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < kOpt / 64; ++c) tc::tmem_st32(tmem + lanes + kTmQ + (kOpt / 2) * hh + 32 * c, r[c]);
         tc::tmem_st_wait();
-        if (rank == 0) {                        // RoPE query part -> smem (bf16 as is, or fp16)
+        {                                       // RoPE query part -> smem (bf16 as is, or fp16)
 #pragma unroll
-          for (int v = 0; v < 8 / kTpr; ++v) {
+          for (int v = 0; v < 4 / kTpr; ++v) {
             if (kRopeF16) {
               qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].x), qpe[v].y);
               qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].z), qpe[v].w);
             }
-            st_unit(sQr, i, (8 / kTpr) * hh + v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+            st_unit64(sQr, i, (4 / kTpr) * hh + v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
           }
           tc::fence_proxy_async();
         }
@@ -773,31 +792,32 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
           ls[e & 3] = tc::add_f16hi_f32(pk[e], tc::add_f16lo_f32(pk[e], ls[e & 3]));
         }
         l_h += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // P.V of tile u-1 has finished: the P buffer is free and O is stable.
-        // (A new item's O restarts with its first P.V: nothing to rescale.)
-        if (u >= 1) {
-          wait_ok(&B.pv_done, (u - 1) & 1);
-          if (!dead && t >= 1) {
+        // P buffer u&1 is free once P.V of tile u-2 has finished; O is stable for
+        // a rescale once P.V of tile u-1 has (waited for only when a rescale is
+        // due).  (A new item's O restarts with its first P.V: nothing to
+        // rescale.)  Each pv_done barrier's phases are followed one by one.
+        if (u >= 2) wait_ok(&B.pv_done[u & 1], ((u >> 1) - 1) & 1);
+        if (!dead && t >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          wait_ok(&B.pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1);
+          if (!dead) {
             tc::fence_after_sync();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-              for (int c = 0; c < kOpt / 32; ++c) {
-                uint32_t o[32];
-                const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
-                tc::tmem_ld32(col, o);
-                tc::tmem_ld_wait();
+            for (int c = 0; c < kOpt / 32; ++c) {
+              uint32_t o[32];
+              const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
+              tc::tmem_ld32(col, o);
+              tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                tc::tmem_st32(col, o);
-              }
-              tc::tmem_st_wait();
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::tmem_st32(col, o);
             }
+            tc::tmem_st_wait();
           }
         }
         if (dead) return;
 #pragma unroll
         for (int g = 0; g < kUpt; ++g)
-          st_unit(sP, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+          st_unit(sP + (u & 1) * kPBytes, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
         tc::fence_proxy_async();
         tc::fence_before_sync();
         mbar_arrive(&B.p_full);
@@ -873,7 +893,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         mbar_arrive(&B.l_ready[k & 1]);
       } else {
         // Decode: O / l -> the fp32 partials, with the running max and sum.
-        wait_ok(&B.pv_done, (u0 + n - 1) & 1);
+        wait_ok(&B.pv_done[(u0 + n - 1) & 1], ((u0 + n - 1) >> 1) & 1);
         group_meet(aux_l, l_h, u0 + n);
         if (!dead) {
           tc::fence_after_sync();
@@ -979,16 +999,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         for (int c = 0; c < 2; ++c) tc::tmem_st32(tmem + lanes + kTmQ + 32 * (2 * h2 + c), r[c]);
       }
       tc::tmem_st_wait();
-      if (rank == 0) {                          // RoPE query part -> smem, fp16
-        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
-        uint4 qpe[8];
+      {                                         // this CTA's 32 RoPE query dims -> smem, fp16
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope) +
+                          4 * rank;
+        uint4 qpe[4];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < 4; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
+        for (int v = 0; v < 4; ++v) {
           qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].x), qpe[v].y);
           qrun = bf16x2_absmax(bf16x2_absmax(qrun, qpe[v].z), qpe[v].w);
-          st_unit(sQr, i, v, bf16x8_to_f16x8(qpe[v]));
+          st_unit64(sQr, i, v, bf16x8_to_f16x8(qpe[v]));
         }
         tc::fence_proxy_async();
       }
@@ -1087,13 +1108,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         for (int c = 0; c < 2; ++c) tc::tmem_st32(tmem + lanes + kTmQ + 32 * (2 * h2 + c), r[c]);
       }
       tc::tmem_st_wait();
-      if (rank == 0) {                          // RoPE query part -> smem (fp16, or bf16 for the bf16 decode)
-        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope);
-        uint4 qpe[8];
+      {                                         // this CTA's 32 RoPE query dims -> smem (fp16, or bf16 for the bf16 decode)
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_pe) + qrow * kRope) +
+                          4 * rank;
+        uint4 qpe[4];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < 4; ++v) qpe[v] = rvalid ? __ldg(qp + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) st_unit(sQr, i, v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
+        for (int v = 0; v < 4; ++v) st_unit64(sQr, i, v, kRopeF16 ? bf16x8_to_f16x8(qpe[v]) : qpe[v]);
         tc::fence_proxy_async();
       }
       tc::fence_before_sync();
@@ -1185,22 +1207,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tc::tma_load_3d(sLat + ls * kLatStage + c * kChunk, &tm_cache, &landed[ls], 256 * rank + 64 * c, key, 0);
-          if (rank == 0) {
-            if (u >= kRopeStages &&
-                !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
-              break;
-            mbar_arrive_expect_tx(&B.rope_full[rs], kChunk);
-            tc::tma_load_3d(sRope + rs * kChunk, &tm_cache, &B.rope_full[rs], kLatent, key, 0);
-          }
+          if (u >= kRopeStages &&
+              !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
+            break;
+          mbar_arrive_expect_tx(&B.rope_full[rs], kRopeChunk);   // this CTA's 32 RoPE dims
+          tc::tma_load_3d(sRope + rs * kRopeChunk, &tm_rope, &B.rope_full[rs], kLatent + kRopeHalf * rank, key, 0);
         }
       }
       // (bf16 decode: the two converter warps after this one run the
       // epilogue warps' conversion loop.)
     } else {
-      if (rank == 0)
-        run_producer<true, true>(&tm_cache, a, B, sLat, sRope, 0, false, pt, first, stride);
-      else
-        run_producer<true, false>(&tm_cache, a, B, sLat, sRope, 1, false, pt, first, stride);
+      run_producer<true, true>(&tm_rope, a, B, sLat, sRope, static_cast<int>(rank), false, pt, first, stride);
     }
   } else {
     // ============================== MMA issue ==================================
@@ -1218,9 +1235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (!wait_all(&B.lat_full[ls], (u / kLatStages) & 1, a)) return false;
       // RoPE tiles by TMA (prefill, bf16 decode); the q8_0 producer writes them
       // with the latent part, under lat_full.
-      if ((!kDecode || !kQ8) && rank == 0 &&
-          !wait_all(&B.rope_full[rs], (u / kRopeStages) & 1, a))
-        return false;
+      if ((!kDecode || !kQ8) && !wait_all(&B.rope_full[rs], (u / kRopeStages) & 1, a)) return false;
       if (u >= 2 && !wait_all(&B.s_free[sb], ((u >> 1) - 1) & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t k0 = smem_u32(sLat + ls * kLatStage);
@@ -1229,12 +1244,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       for (int ks = 0; ks < 16; ++ks)        // latent half: A = Q from TMEM
         tc::mma_ts_warp(d, tmem + kTmQ + ks * 8, tc::sdesc_sw128(k0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024),
                         idesc_lat, ks > 0 ? 1u : 0u);
-      if (rank == 0) {
-        const uint32_t q0 = smem_u32(sQr), r0 = smem_u32(sRope + rs * kChunk);
+      {                                      // RoPE part, this CTA's 32 dims: A = Q_pe from smem
+        const uint32_t q0 = smem_u32(sQr), r0 = smem_u32(sRope + rs * kRopeChunk);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)       // RoPE part: A = Q_pe from smem
-          tc::mma_ss_warp(d, tc::sdesc_sw128(q0 + ks * 32, 16, 1024), tc::sdesc_sw128(r0 + ks * 32, 16, 1024),
-                          idesc_rope, 1u);
+        for (int ks = 0; ks < kRopeHalf / 16; ++ks)
+          tc::mma_ss_warp(d, tc::sdesc_sw64(q0 + ks * 32), tc::sdesc_sw64(r0 + ks * 32), idesc_rope, 1u);
         tc::mma_commit_warp(&B.rope_empty[rs]);
       }
       tc::mma_commit_warp(&B.s_full[sb]);
@@ -1247,13 +1261,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (t0 && k > 0 && !wait_all(&B.o_free, (k - 1) & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t v0 = smem_u32(sLat + (u % kLatStages) * kLatStage);
-      const uint32_t p0 = smem_u32(sP);
+      const uint32_t p0 = smem_u32(sP + (u & 1) * kPBytes);
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks)
         tc::mma_ss_warp(tmem + kTmO, tc::sdesc_sw128(p0 + ks * 32, 16, 1024),
                         tc::sdesc_sw128(v0 + ks * 2048, kChunk, 1024), idesc_pv, (!t0 || ks > 0) ? 1u : 0u);
       tc::mma_commit_warp(&B.lat_empty[u % kLatStages]);
-      tc::mma_commit_warp(&B.pv_done);
+      tc::mma_commit_warp(&B.pv_done[u & 1]);
       return true;
     };
     if constexpr (mma_warps(kQ8, kDecode) == 2) {
@@ -1319,11 +1333,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 }
 
 template <bool kQ8, bool kDecode>
-cudaError_t launch_one(const CUtensorMap& tm, const AttnTcArgs& a, int n_clusters, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& tm, const CUtensorMap& tm_rope, const AttnTcArgs& a, int n_clusters,
+                       cudaStream_t stream) {
   auto kern = attn_tc_kernel<kQ8, kDecode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(2 * n_clusters), threads(kQ8, kDecode), kSmem, stream>>>(tm, a);
+  kern<<<dim3(2 * n_clusters), threads(kQ8, kDecode), kSmem, stream>>>(tm, tm_rope, a);
   return cudaGetLastError();
 }
 
@@ -1345,16 +1360,22 @@ cudaError_t launch_attn_tc(const AttnTcArgs& args, bool q8, bool decode, int n_i
   // Tensor map of the cache rows the kernel may address (64 dims x 64 keys
   // boxes, 128-byte swizzle; rows past n_rows read as zero): the fp16 staging
   // copy for a prefill, the bf16 cache (RoPE tiles) for a bf16 decode.
-  CUtensorMap tm;
+  // The RoPE part (32 dims x 64 keys per CTA) through a second map with 64-byte
+  // swizzle.
+  CUtensorMap tm, tm_rope;
   if (!decode || !q8) {
     const uint64_t rows = static_cast<uint64_t>(a.n_rows);
     cudaError_t e = make_tmap_3d(&tm, a.kv, decode, kRow, rows, 1, kRow * 2, rows * kRow * 2, 64, kBK, 1);
     if (e != cudaSuccess) return e;
+    e = make_tmap_3d(&tm_rope, a.kv, decode, kRow, rows, 1, kRow * 2, rows * kRow * 2, kRopeHalf, kBK, 1, 64);
+    if (e != cudaSuccess) return e;
   } else {
     memset(&tm, 0, sizeof(tm));
+    memset(&tm_rope, 0, sizeof(tm_rope));
   }
-  if (!decode) return launch_one<false, false>(tm, a, n_clusters, stream);
-  return q8 ? launch_one<true, true>(tm, a, n_clusters, stream) : launch_one<false, true>(tm, a, n_clusters, stream);
+  if (!decode) return launch_one<false, false>(tm, tm_rope, a, n_clusters, stream);
+  return q8 ? launch_one<true, true>(tm, tm_rope, a, n_clusters, stream)
+            : launch_one<false, true>(tm, tm_rope, a, n_clusters, stream);
 }
 
 }  // namespace mla

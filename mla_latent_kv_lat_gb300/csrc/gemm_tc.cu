@@ -238,9 +238,10 @@ cudaError_t get_tmap_encoder(void** fn) {
   return cudaSuccess;
 }
 
-// 3-D tiled tensor map, 16-bit elements, 128-byte swizzle, zero fill outside.
+// 3-D tiled tensor map, 16-bit elements, 128-byte (or 64-byte) swizzle, zero fill outside.
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
-                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         int swizzle_bytes) {
   void* fn = nullptr;
   cudaError_t e = get_tmap_encoder(&fn);
   if (e != cudaSuccess) return e;
@@ -250,7 +251,8 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)(
       map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
-      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

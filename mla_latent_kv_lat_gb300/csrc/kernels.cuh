@@ -78,9 +78,11 @@ struct AttnTcArgs {
   int n_items;              // set by launch_attn_tc
 };
 
-// 3-D tiled tensor map of 16-bit elements with 128-byte swizzle (zero fill outside).
+// 3-D tiled tensor map of 16-bit elements with 128-byte swizzle, or 64-byte
+// with swizzle_bytes = 64 (zero fill outside).
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
-                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         int swizzle_bytes = 128);
 
 // Prefill: n_items row tiles of 128.  Decode: n_items = number of clusters G
 // (the pieces are found on the device).

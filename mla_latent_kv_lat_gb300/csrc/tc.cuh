@@ -100,6 +100,13 @@ MLA_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same for a 64-byte-swizzled K-major tile: rows of 32 16-bit elements
+// (64 B), 8-row groups 512 B apart, layout SWIZZLE_64B = 4 in bits 61-63.
+MLA_DEVINL uint64_t sdesc_sw64(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(512 >> 4) << 32) | (1ull << 46) | (4ull << 61);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with fp32 accumulation:
 // D format F32 (bits 4-5 = 1), A/B format (bits 7-9, 10-12: 0 = F16,
 // 1 = BF16), A/B major (bit 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 in
