@@ -52,7 +52,9 @@ SECONDARY_WORKLOADS = ["lite_t4096", "lite_t256", "v3_decode_b32", "v3_q8_chunk8
 FLOP_PER_PAIR_HEAD = 2 * 576 + 2 * 512          # scores (576-d) + latent weighted sum (512-d)
 # sources whose hash dates the ncu traffic recorded for each kernel
 KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"],
-                  "rope_append_kernel": ["append.cu", "append.cuh", "common.cuh"]}
+                  "rope_append_kernel": ["append.cu", "append.cuh", "common.cuh"],
+                  "pp_attn_tc_kernel": ["materialize.cu", "tc.cuh", "common.cuh", "kernels.cuh"],
+                  "wo_gemm_tc_kernel": ["wo_tc.cu", "tc.cuh", "common.cuh", "kernels.cuh"]}
 
 
 # ---------------------------------------------------------------------------
@@ -294,7 +296,9 @@ def measure_variant(args, torch, full, flush, pk, pk_kind, world=1):
                     "roofline": {"bound": "tensor", "achieved": round(own, 3), "peak": peak, "unit": "TFLOP/s",
                                  "frac": round(own / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst",
                                  "kernel": "pp_prep_kernel+pp_decompress_tc_kernel+pp_attn_tc_kernel",
-                                 "attn_ms": round(kms, 4), "traffic": None}})
+                                 "attn_ms": round(kms, 4),
+                                 "traffic": recorded_traffic("pp_attn_tc_kernel", full),
+                                 "traffic_kernel": "pp_attn_tc_kernel (the call's dominant kernel)"}})
         out["e2e"] = e2e_generic(args, torch, d, step, bufs[0], materialized_flops(wl), 1e12, "TFLOP/s")
     else:
         tf = wo_flops(wl) / (kms * 1e-3) / 1e12
@@ -303,7 +307,8 @@ def measure_variant(args, torch, full, flush, pk, pk_kind, world=1):
                     "hidden": wl.hidden,
                     "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak, "unit": "TFLOP/s",
                                  "frac": round(tf / peak, 4), "peak_kind": f"{pk_kind} bf16 dense, burst",
-                                 "kernel": "wo_gemm_tc_kernel", "attn_ms": round(kms, 4), "traffic": None,
+                                 "kernel": "wo_gemm_tc_kernel", "attn_ms": round(kms, 4),
+                                 "traffic": recorded_traffic("wo_gemm_tc_kernel", full),
                                  "flops": wo_flops(wl)}})
     del d, bufs, step
     return out
