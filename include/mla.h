@@ -148,11 +148,10 @@ int mla_attn_prefill_q8_0(const mla_dims* dims, const void* q_lat, const void* q
 
 /* Bytes of device workspace mla_attn_prefill_materialized needs for a chunk
  * of T queries at positions q_pos0.. with head_chunk heads decompressed at a
- * time (0 = all n_head): fp16 queries (T rounded up to 128, x H x 384 bytes),
- * fp16 RoPE keys (128 bytes a row), for one head chunk fp16 keys and values
- * (512 bytes a row and head), and for a q8_0 cache an fp16 copy of its rows
- * (1152 bytes a row), for the q_pos0 + T rows a chunk reads.  The size serves
- * either cache type.  Returns 0 for invalid arguments.                        */
+ * time (0 = all n_head): for one head chunk the fp16 keys (nope part) and
+ * values (512 bytes a row and head), and for a q8_0 cache an fp16 copy of its
+ * rows (1152 bytes a row), for the q_pos0 + T rows a chunk reads.  The size
+ * serves either cache type.  Returns 0 for invalid arguments.                 */
 size_t mla_prefill_materialized_workspace_size(const mla_dims* dims, int32_t T, int32_t q_pos0,
                                                int32_t head_chunk);
 
@@ -173,8 +172,9 @@ size_t mla_prefill_materialized_workspace_size(const mla_dims* dims, int32_t T, 
  * workspace device, ws_bytes >= mla_prefill_materialized_workspace_size(...)
  * o      device fp32 [T][H][128] output;  lse fp32 [T][H] or NULL
  * Requires T >= 1, q_pos0 >= 0, q_pos0 + T <= n_kv; rows past q_pos0 + T - 1
- * are never read.  Keys, values, queries and probabilities are fp16 tensor-
- * core operands (fp32 accumulation); the fp16 range rules above apply.        */
+ * are never read.  The nope parts of keys and queries, the values and the
+ * probabilities are fp16 tensor-core operands, the RoPE parts the bf16 values
+ * as given (fp32 accumulation); the fp16 range rules above apply.             */
 int mla_attn_prefill_materialized(const mla_dims* dims, const void* q_nope, const void* q_pe,
                                   const void* kv, const void* wk_b, const void* wv_b, int32_t n_kv,
                                   int32_t T, int32_t q_pos0, int32_t head_chunk, void* workspace,

@@ -8,70 +8,29 @@
 // FLOPs than the absorbed form (640 vs 2176 per visible pair and head, plus
 // 256 x 512 x 2 per cache row and head for the decompression).
 //
-// Three kernels per head chunk of hc heads:
-//   prep        q_nope | q_pe (bf16) -> Q16, fp16, laid out so that each
-//               TMEM row load is one coalesced 512-byte read; k_pe -> fp16.
+// Two kernels per head chunk of hc heads:
 //   decompress  K16[j][h] = c_kv[j] . wk_b[h]^T and V16[j][h] = c_kv[j] . wv_b[h]
 //               (tcgen05, bf16 x bf16 -> fp32, rounded once to fp16).
 //   attention   one head x 128 query rows per item, keys in tiles of 128:
-//               S = Q K^T (Q in TMEM, K from a 3-stage TMA ring), causal
+//               S = Q K^T (Q in TMEM, K from a 3-stage TMA ring: the nope part
+//               from K16, the RoPE part straight from the cache), causal
 //               online softmax (8 warps, two threads per row), P written back
 //               over S in TMEM as fp16 and used there as the A operand of
 //               O += P V (V from a 2-stage ring); 4 warps load each item's Q
+//               (q_nope converted to fp16, q_pe as the cache's RoPE keys are)
 //               into TMEM and write the previous item's o = O / l.
-// fp16 operands for the same reason as the absorbed path: bf16 keys alone
-// would cost ~1.5e-3 of the 2e-3 mean relative error budget.
+// The nope keys, values, queries and P are fp16 for the same reason as the
+// absorbed path: bf16 keys alone would cost ~1.5e-3 of the 2e-3 mean relative
+// error budget.  The RoPE part of the scores multiplies the bf16 q_pe and k_pe
+// as they are (with a q8_0 cache: the fp16 staged keys and fp16 q_pe).
 #include "kernels.cuh"
 #include "tc.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kQUnits = (kNope + kRope) / 8;     // 24 16-byte units of a 192-wide fp16 query row
 constexpr int kFR = 128;                          // query rows per item (MMA M)
 constexpr int kFN = 128;                          // keys per tile (MMA N of Q K^T)
-
-// ---------------------------------------------------------------------------
-// prep: Q16 unit u of row i of item (query tile qt, head h) is uint4 number
-// ((qt * H + h) * 24 + u) * 128 + i; rows past T are zero.  kpe16 [rows][64].
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) pp_prep_kernel(const uint4* q_nope, const uint4* q_pe, const uint4* kv,
-                                                      uint4* q16, uint4* kpe16, int T, int H, int n_qt,
-                                                      int64_t rows, int* err) {
-  const int64_t nq = static_cast<int64_t>(n_qt) * kFR * H * kQUnits;
-  const int64_t nk = kv != nullptr ? rows * (kRope / 8) : 0;   // q8_0: none (read from the fp16 staging copy)
-  uint32_t run = 0;
-  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < nq + nk;
-       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    int64_t dst;
-    if (x < nq) {                      // reads in (t, h, u) order, u fastest: coalesced
-      const int u = static_cast<int>(x % kQUnits);
-      const int64_t th = x / kQUnits;
-      const int h = static_cast<int>(th % H);
-      const int64_t t = th / H;
-      if (t < T) v = u < 16 ? __ldg(q_nope + th * 16 + u) : __ldg(q_pe + th * 8 + (u - 16));
-      dst = ((t / kFR * H + h) * kQUnits + u) * kFR + t % kFR;
-    } else {
-      const int64_t y = x - nq;
-      v = __ldg(kv + (y >> 3) * (kRow / 8) + kLatent / 8 + (y & 7));
-      dst = -1 - y;
-    }
-    run = bf16x2_absmax(bf16x2_absmax(run, v.x), v.y);
-    run = bf16x2_absmax(bf16x2_absmax(run, v.z), v.w);
-    uint4 o;
-    float2 f;
-    f = bf16x2_to_f32(v.x); o.x = pack_f16x2(f.x, f.y);
-    f = bf16x2_to_f32(v.y); o.y = pack_f16x2(f.x, f.y);
-    f = bf16x2_to_f32(v.z); o.z = pack_f16x2(f.x, f.y);
-    f = bf16x2_to_f32(v.w); o.w = pack_f16x2(f.x, f.y);
-    if (dst >= 0)
-      q16[dst] = o;
-    else
-      kpe16[-1 - dst] = o;
-  }
-  if (bf16x2_absmax_overflows(run)) record_error(err, MLA_ERR_RANGE);
-}
 
 // ---------------------------------------------------------------------------
 // decompress: CTA (head hl of the chunk, part p, row group g); part 0 makes
@@ -82,11 +41,12 @@ __global__ void __launch_bounds__(256) pp_prep_kernel(const uint4* q_nope, const
 // converted to fp16 in shared memory by the epilogue warps before the first
 // MMA (both operands of an MMA have one type).
 // ---------------------------------------------------------------------------
-constexpr int kDStages = 4;
+constexpr int kDStages = 5;   // a chunk's MMAs take ~340 cycles: five stages cover the TMA latency
 constexpr int kDChunk = 128 * 128;                // 16 KB: 128 rows x 64 bf16
 constexpr int kDWBytes = 128 * 1024;              // W: 512 x 128 bf16
 constexpr int kDStgBytes = 4 * 2048;
 constexpr int kDSmem = 1024 + kDWBytes + kDStages * kDChunk + kDStgBytes + 256;
+static_assert(kDSmem <= 232448, "shared memory");
 constexpr int kDThreads = 192;
 
 struct DecompArgs {
@@ -299,7 +259,8 @@ constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 384;
 constexpr float kFRescale = 8.0f;
 
 struct FaArgs {
-  const uint4* q16;
+  const uint16_t* q_nope;   // bf16 [T][H][128]
+  const uint16_t* q_pe;     // bf16 [T][H][64]
   float* o;            // fp32 [T][H][128]
   float* lse;          // fp32 [T][H] or null
   int T, H, q_pos0, h0, hc, n_qt, n_items;
@@ -339,6 +300,7 @@ struct FaBars {
   uint32_t tmem;
 };
 
+template <bool kRopeBf16>
 __global__ void __launch_bounds__(kFThreads, 1)
     pp_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmR, FaArgs a) {
@@ -527,6 +489,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     };
     FaItem prev;
     int k = 0;
+    uint32_t qrun = 0;                            // query values converted to fp16: range check
 #pragma unroll 1
     for (int rnd = 0; ok && rnd * stride < a.n_items; ++rnd) {
       const int idx = fa_round_item(first, stride, rnd);
@@ -535,13 +498,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
       if (k > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&B.q_free, (k - 1) & 1, a.wait_us, a.err));
       if (!ok) break;
       tc::fence_after_sync();
-      const uint4* src = a.q16 + (static_cast<int64_t>(it.t0 / kFR) * a.H + a.h0 + it.hl) * kQUnits * kFR + i;
+      // Q row i: q_nope as fp16 (TMEM columns 0-63), q_pe as the RoPE keys are
+      // stored (columns 64-95).  Once per item of ~300 key tiles, so the loads
+      // need not be coalesced.
+      const bool rvalid = i < it.nvalid;
+      const int64_t th = static_cast<int64_t>(it.t0 + i) * a.H + a.h0 + it.hl;
+      const uint4* qn = reinterpret_cast<const uint4*>(a.q_nope + th * kNope);
+      const uint4* qp = reinterpret_cast<const uint4*>(a.q_pe + th * kRope);
 #pragma unroll 1
       for (int c = 0; c < 3; ++c) {               // 8 units = 32 TMEM columns per step
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x = __ldg(src + (8 * c + v) * kFR);
+          uint4 x = rvalid ? __ldg(c < 2 ? qn + 8 * c + v : qp + v) : make_uint4(0, 0, 0, 0);
+          if (c < 2 || !kRopeBf16) {
+            qrun = bf16x2_absmax(bf16x2_absmax(qrun, x.x), x.y);
+            qrun = bf16x2_absmax(bf16x2_absmax(qrun, x.z), x.w);
+            uint4 y;
+            float2 f;
+            f = bf16x2_to_f32(x.x); y.x = pack_f16x2(f.x, f.y);
+            f = bf16x2_to_f32(x.y); y.y = pack_f16x2(f.x, f.y);
+            f = bf16x2_to_f32(x.z); y.z = pack_f16x2(f.x, f.y);
+            f = bf16x2_to_f32(x.w); y.w = pack_f16x2(f.x, f.y);
+            x = y;
+          }
           r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
         }
         tc::tmem_st32(tmem + lanes + kTmQ + 32 * c, r);
@@ -554,6 +534,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       ++k;
     }
     if (ok && k > 0) epilogue(prev, k - 1);
+    if (bf16x2_absmax_overflows(qrun)) record_error(a.err, MLA_ERR_RANGE);
   } else if (warp == kFLoadWarp) {
     // ============================== loader =====================================
     if (lane == 0) {
@@ -594,6 +575,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // ...: the tensor core runs them in issue order, so QK(u + 2), which
     // overwrites the score buffer holding P(u), always follows PV(u).
     constexpr uint32_t idesc_qk = tc::idesc_f16(kFR, kFN, false, false, false);
+    constexpr uint32_t idesc_rope = tc::idesc_f16(kFR, kFN, kRopeBf16, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_f16(kFR, kVHead, false, false, true);
     bool ok = true;
     auto issue_qk = [&](int u) {
@@ -605,7 +587,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
       for (int s = 0; s < 12; ++s)
         tc::mma_ts_warp(tmem + kTmS + sb * 128, tmem + kTmQ + s * 8,
-                        tc::sdesc_sw128(k0 + (s >> 2) * kKChunk + (s & 3) * 32, 16, 1024), idesc_qk, s > 0 ? 1u : 0u);
+                        tc::sdesc_sw128(k0 + (s >> 2) * kKChunk + (s & 3) * 32, 16, 1024), s < 8 ? idesc_qk : idesc_rope,
+                        s > 0 ? 1u : 0u);
       tc::mma_commit_warp(&B.k_empty[ks]);
       tc::mma_commit_warp(&B.s_full[sb]);
     };
@@ -656,21 +639,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 }
 
-unsigned grid_for(int64_t n_units) {
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
-  return static_cast<unsigned>(max(static_cast<int64_t>(1), min(cap, (n_units + 255) / 256)));
-}
 
 }  // namespace
 
-// Workspace: Q16 (all heads), kpe16, K16 and V16 of one head chunk, and for
-// a q8_0 cache the fp16 staging copy of its rows.
+// Workspace: K16 and V16 of one head chunk and, for a q8_0 cache, the fp16
+// staging copy of its rows.
 size_t pp_workspace_bytes(int H, int32_t T, int32_t q_pos0, int hc, bool q8) {
+  (void)H;
   auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
-  const size_t n_qt = (static_cast<size_t>(T) + kFR - 1) / kFR;
   const size_t rows = static_cast<size_t>(q_pos0) + T;
-  return up(n_qt * H * kQUnits * kFR * 16) + up(rows * kRope * 2) + 2 * up(rows * hc * kVHead * 2) +
-         (q8 ? up(rows * kRow * 2) : 0);
+  return 2 * up(rows * hc * kVHead * 2) + (q8 ? up(rows * kRow * 2) : 0);
 }
 
 cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
@@ -679,10 +657,6 @@ cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
   const int n_qt = (T + kFR - 1) / kFR;
   const int64_t rows = static_cast<int64_t>(p.q_pos0) + T;     // rows past the last query are never read
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
-  uint4* q16 = reinterpret_cast<uint4*>(ws);
-  ws += up(static_cast<size_t>(n_qt) * H * kQUnits * kFR * 16);
-  uint4* kpe16 = reinterpret_cast<uint4*>(ws);
-  ws += up(static_cast<size_t>(rows) * kRope * 2);
   uint16_t* k16 = reinterpret_cast<uint16_t*>(ws);
   ws += up(static_cast<size_t>(rows) * p.hc * kVHead * 2);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws);
@@ -698,13 +672,6 @@ cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     rows_src = staged;
   }
-  const int64_t n_units = static_cast<int64_t>(n_qt) * kFR * H * kQUnits + (q8 ? 0 : rows * (kRope / 8));
-  pp_prep_kernel<<<grid_for(n_units), 256, 0, stream>>>(static_cast<const uint4*>(p.q_nope),
-                                                       static_cast<const uint4*>(p.q_pe),
-                                                       static_cast<const uint4*>(p.kv), q16, kpe16, T, H, n_qt,
-                                                       rows, p.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
 
   CUtensorMap tmA, tmWk, tmWv, tmK, tmV, tmR;
   e = make_tmap_3d(&tmA, rows_src, !q8, kRow, static_cast<uint64_t>(rows), 1, kRow * 2,
@@ -714,16 +681,16 @@ cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_tmap_3d(&tmWv, p.wv_b, true, kVHead, kLatent, H, kVHead * 2, kLatent * kVHead * 2, 64, 256, 1);
   if (e != cudaSuccess) return e;
-  if (q8)   // the RoPE part of the staged rows: base at column 512, row stride 1152 bytes
-    e = make_tmap_3d(&tmR, static_cast<const uint16_t*>(rows_src) + kLatent, false, kRope, 1,
-                     static_cast<uint64_t>(rows), kRow * 2, kRow * 2, 64, 1, kFN);
-  else
-    e = make_tmap_3d(&tmR, kpe16, false, kRope, 1, static_cast<uint64_t>(rows), kRope * 2, kRope * 2, 64, 1, kFN);
+  // the RoPE keys: columns 512-575 of the rows (bf16 cache, or the fp16 staged
+  // rows of a q8_0 cache), base at column 512, row stride 1152 bytes
+  e = make_tmap_3d(&tmR, static_cast<const uint16_t*>(rows_src) + kLatent, !q8, kRope, 1,
+                   static_cast<uint64_t>(rows), kRow * 2, kRow * 2, 64, 1, kFN);
   if (e != cudaSuccess) return e;
   auto decomp = q8 ? pp_decompress_tc_kernel<true> : pp_decompress_tc_kernel<false>;
   e = cudaFuncSetAttribute(decomp, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(pp_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+  auto attn = q8 ? pp_attn_tc_kernel<false> : pp_attn_tc_kernel<true>;
+  e = cudaFuncSetAttribute(attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int row_tiles = static_cast<int>((rows + 127) / 128);
@@ -751,7 +718,8 @@ cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     FaArgs f;
-    f.q16 = q16;
+    f.q_nope = static_cast<const uint16_t*>(p.q_nope);
+    f.q_pe = static_cast<const uint16_t*>(p.q_pe);
     f.o = p.o;
     f.lse = p.lse;
     f.T = T;
@@ -765,7 +733,7 @@ cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream) {
     f.err = p.err;
     f.wait_us = p.wait_us;
     const int grid = min(f.n_items, sms);
-    pp_attn_tc_kernel<<<grid, kFThreads, kFSmem, stream>>>(tmK, tmV, tmR, f);
+    attn<<<grid, kFThreads, kFSmem, stream>>>(tmK, tmV, tmR, f);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

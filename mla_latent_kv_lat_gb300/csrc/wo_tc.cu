@@ -5,8 +5,9 @@
 // wo, the einsum hdD,bhqd->bqD).  One dense GEMM, C[M][N] = A[M][K] B[K][N]
 // with M = tokens, K = n_head * 128, N = the hidden size.
 //
-// Persistent CTAs, one per SM, walk 128 x 256 output tiles (M fastest, so the
-// CTAs running at one time share the B columns they read).  Per tile, K moves
+// Persistent CTAs, one per SM, walk 128 x 256 output tiles in groups of 16 row
+// tiles (within a group M fastest): the ~152 tiles in flight then read about
+// 16 row tiles of A and 10 column tiles of B, ~140 MB, which L2 holds.  Per tile, K moves
 // in 64-wide steps through a 4-stage TMA ring (A: 128 x 64, K-major; B: 64 x
 // 256, N-major, four 64-column boxes), 128-byte swizzled, on tcgen05 MMAs
 // (M = 128, N = 256, K = 16, bf16 x bf16 -> fp32) into one of two TMEM
@@ -39,6 +40,17 @@ struct WoArgs {
   int* err;
   uint32_t wait_us;
 };
+
+constexpr int kGroupM = 16;
+
+// Output tile t -> (row, column) of its first element.
+MLA_DEVINL void wo_tile(const WoArgs& g, int t, int& m0, int& n0) {
+  const int per_group = kGroupM * g.n_tiles;
+  const int grp = t / per_group, w = t % per_group;
+  const int rows = min(kGroupM, g.m_tiles - grp * kGroupM);
+  m0 = (grp * kGroupM + w % rows) * kBM;
+  n0 = (w / rows) * kBN;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     wo_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, WoArgs g) {
@@ -84,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u = 0;                                   // k-steps issued, across tiles
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const int m0 = (t % g.m_tiles) * kBM, n0 = (t / g.m_tiles) * kBN;
+        int m0, n0;
+        wo_tile(g, t, m0, n0);
         for (int kc = 0; kc < kc_n; ++kc, ++u) {
           const int st = u % kStages;
           if (u >= kStages && !mbar_wait_bounded(&empty[st], ((u / kStages) - 1) & 1, g.wait_us, g.err)) {
@@ -133,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int i = 0;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
       const int buf = i & 1;
-      const int m0 = (t % g.m_tiles) * kBM, n0 = (t / g.m_tiles) * kBN;
+      int m0, n0;
+      wo_tile(g, t, m0, n0);
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, g.wait_us, g.err));
       if (!ok) break;
       tc::fence_after_sync();
