@@ -135,3 +135,59 @@ def mla_prefill_host(host: dict, q_pos0: int, dev: dict, bufs: PrefillBuffers, o
                 kv_q=dev.get("kv_q"), kv_d=dev.get("kv_d"), bufs=bufs, stream=stream)
     out_host.copy_(bufs.o, non_blocking=True)
     return out_host
+
+
+class HostOverlap:
+    """Steps of the path on pinned host buffers, with the copies overlapped.
+
+    Every step copies its inputs host -> device and its output device -> host,
+    but on a copy stream of their own: step k+1's inputs go in and step k-1's
+    output comes out while step k computes on the compute stream.  Two device
+    input sets and two device outputs alternate; events order each copy
+    against the steps that use its buffers.  ``step(dev, out)`` enqueues one
+    step's kernels on the current stream, reading the input tensors in the
+    dict ``dev`` and writing ``out``.
+    """
+
+    def __init__(self, host: dict, dev_sets, outs, step):
+        self.host = host
+        self.dev = dev_sets                     # two dicts of device inputs (same keys as host)
+        self.outs = outs                        # two device outputs
+        self.step = step
+        self.host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        self.copy = torch.cuda.Stream()
+        self.compute = torch.cuda.Stream()
+
+    def run(self, n: int) -> float:
+        """Run n steps; return the milliseconds from the first copy in to the
+        last copy out (CUDA events)."""
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+
+        def copy_in(k):
+            s = k % 2
+            with torch.cuda.stream(self.copy):
+                if k >= 2:
+                    self.copy.wait_event(ev_done[s])      # step k-2 no longer reads this input set
+                for key, t in self.host.items():
+                    self.dev[s][key].copy_(t, non_blocking=True)
+                ev_in[s].record(self.copy)
+
+        t0.record(self.copy)
+        copy_in(0)
+        for k in range(n):
+            s = k % 2
+            with torch.cuda.stream(self.compute):
+                self.compute.wait_event(ev_in[s])
+                self.step(self.dev[s], self.outs[s])
+                ev_done[s].record(self.compute)
+            if k + 1 < n:
+                copy_in(k + 1)
+            with torch.cuda.stream(self.copy):
+                self.copy.wait_event(ev_done[s])
+                self.host_out[s].copy_(self.outs[s], non_blocking=True)
+        t1.record(self.copy)
+        t1.synchronize()
+        return t0.elapsed_time(t1)

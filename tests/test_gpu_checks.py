@@ -5,7 +5,9 @@
   device error word, never silently turned into inf or NaN downstream;
 * the decode's sequence table: a sequence that names rows outside the cache,
   an empty one or one longer than max_len is skipped and reported as
-  MLA_ERR_INVALID_ARG, and the other sequences still match the oracle.
+  MLA_ERR_INVALID_ARG, and the other sequences still match the oracle;
+* host buffers with the copies overlapped (pipeline.HostOverlap, the bench's
+  end-to-end leg): every step's output equals the plain device call's.
 
 Every case stays inside the allocated tensors (a sequence that runs past the
 cache's n_rows still ends inside the buffer), so none can fault even if a
@@ -151,3 +153,28 @@ def test_decode_skips_and_reports_bad_sequences(q8):
     assert_tol(got[good], ref, tol, "valid sequences beside skipped ones")
     assert not got[[1, 2, 4]].any()                # skipped: left as they were (zeros)
     assert mla.mla_get_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# Host buffers with overlapped copies (pipeline.HostOverlap)
+# ---------------------------------------------------------------------------
+def test_host_overlap_gives_the_serial_results():
+    from mla_latent_kv_lat_gb300 import pipeline as P
+    x = W.make_inputs("lite_t256", T=200, q_pos0=56, n_kv=256)
+    d0 = Dev(x)
+    ref = mla.mla_prefill(d0.q_nope, d0.q_pe, d0.wk_b, d0.wv_b, 56, kv=d0.kv).o.clone()
+    d = {"q_nope": d0.q_nope, "q_pe": d0.q_pe, "wk_b": d0.wk_b, "wv_b": d0.wv_b, "kv": d0.kv}
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    bufs = P.prefill_buffers(200, 16, n_kv=256)
+
+    def step(dv, out):
+        P.mla_prefill(dv["q_nope"], dv["q_pe"], dv["wk_b"], dv["wv_b"], 56, kv=dv["kv"],
+                      bufs=P.PrefillBuffers(bufs.q_lat, bufs.o_lat, out, None, bufs.workspace))
+    dev = [{k: torch.zeros_like(v) for k, v in d.items()} for _ in range(2)]
+    outs = [torch.full_like(ref, float("nan")) for _ in range(2)]
+    run = P.HostOverlap(host, dev, outs, step)
+    ms = run.run(5)
+    assert ms > 0
+    assert mla.mla_get_device_error() == 0
+    for s in range(2):                            # both slots ran the step on the copied inputs
+        assert torch.equal(run.host_out[s], ref.cpu())
