@@ -261,18 +261,25 @@ int mla_attn_decode_static(const mla_dims* dims, const void* q_lat, const void* 
 int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_b,
                         float* o, int32_t T, void* stream);
 
-/* As mla_late_decompress, with o rounded once to bf16 (the type the output
- * projection below takes): o device bf16 [T][H][128].                         */
-int mla_late_decompress_bf16(const mla_dims* dims, const void* o_lat, const void* wv_b,
-                             void* o, int32_t T, void* stream);
+/* As mla_late_decompress, with o rounded once to fp16 (the type the output
+ * projection below takes; bf16 would cost about 1.6e-3 mean relative error
+ * of u by itself): o device fp16 [T][H][128].                                  */
+int mla_late_decompress_f16(const mla_dims* dims, const void* o_lat, const void* wv_b,
+                            void* o, int32_t T, void* stream);
+
+/* Weight preparation, once per model load: dst = fp16(src) for n bf16 values
+ * (n a multiple of 8), e.g. the output projection's w_o.  Exact for values in
+ * fp16's normal range; a value fp16 cannot hold records MLA_ERR_RANGE.        */
+int mla_convert_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream);
 
 /* The step after the path, the attention output projection (method page
  * sec. 4: the heads' outputs, flattened to H * 128, times wo -- the einsum
  * hdD,bhqd->bqD; the V up-projection stays a separate, earlier step):
  *   u[t][n] = sum_h sum_e o[t][h][e] * w_o[h][e][n]
- * o    device bf16 [T][H][128]   (mla_late_decompress_bf16's output)
- * w_o  device bf16 [H][128][D]   (row-major [H*128][D])
- * u    device fp32 [T][D]        output, fp32 accumulation
+ * o    device fp16 [T][H][128]   (mla_late_decompress_f16's output)
+ * w_o  device fp16 [H][128][D]   (row-major [H*128][D]; the model's bf16
+ *                                 weight converted once, mla_convert_bf16_to_f16)
+ * u    device fp32 [T][D]        output, fp16 x fp16 products, fp32 accumulation
  * T >= 1; D (the hidden size) a multiple of 64, at most 1<<20
  * (MLA_ERR_UNSUPPORTED otherwise).  A dense GEMM on the tensor cores.         */
 int mla_output_project(const mla_dims* dims, const void* o, const void* w_o, float* u,

@@ -9,7 +9,7 @@ from .binding import (MLAError, declared_symbols, library_path, load_library, ma
                       mla_attn_prefill, mla_attn_prefill_materialized, mla_attn_prefill_materialized_q8_0,
                       mla_prefill_materialized_workspace_size,
                       mla_attn_prefill_q8_0, mla_decode_workspace_size, mla_prefill_workspace_size, mla_get_device_error,
-                      mla_late_decompress, mla_late_decompress_bf16, mla_output_project, mla_quantize_q8_0, mla_rope_append, mla_selftest_wait_timeout,
+                      mla_late_decompress, mla_late_decompress_f16, mla_convert_bf16_to_f16, mla_output_project, mla_quantize_q8_0, mla_rope_append, mla_selftest_wait_timeout,
                       mla_status_string,
                       mla_version)
 from .pipeline import mla_decode, mla_prefill, mla_prefill_projected  # noqa: F401

@@ -60,7 +60,8 @@ _SIGS = {
     "mla_attn_decode_q8_0": ([_D, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
     "mla_attn_decode_static": ([_D, _P, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P], ctypes.c_int),
     "mla_late_decompress": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
-    "mla_late_decompress_bf16": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "mla_late_decompress_f16": ([_D, _P, _P, _P, _I32, _P], ctypes.c_int),
+    "mla_convert_bf16_to_f16": ([_P, _P, _I64, _P], ctypes.c_int),
     "mla_output_project": ([_D, _P, _P, _P, _I32, _I32, _P], ctypes.c_int),
     "mla_quantize_q8_0": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "mla_rope_append": ([_P, _P, _P, _P, _I32, ctypes.c_float, ctypes.c_float, _P, _P, _P, _I64, _I64, _P],
@@ -140,22 +141,31 @@ def mla_late_decompress(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor
     _check("mla_late_decompress", load_library().mla_late_decompress(ctypes.byref(d), *args, T, _stream(stream)))
 
 
-def mla_late_decompress_bf16(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor, scale=None, stream=None):
+def mla_late_decompress_f16(o_lat: torch.Tensor, wv_b: torch.Tensor, o: torch.Tensor, scale=None, stream=None):
     T, H = o_lat.shape[0], o_lat.shape[1]
     d = make_dims(H, scale)
     args = (_need(o_lat, "o_lat", torch.float16, (T, H, KV_LORA_RANK)),
             _need(wv_b, "wv_b", torch.bfloat16, (H, KV_LORA_RANK, V_HEAD)),
-            _need(o, "o", torch.bfloat16, (T, H, V_HEAD)))
-    _check("mla_late_decompress_bf16",
-           load_library().mla_late_decompress_bf16(ctypes.byref(d), *args, T, _stream(stream)))
+            _need(o, "o", torch.float16, (T, H, V_HEAD)))
+    _check("mla_late_decompress_f16",
+           load_library().mla_late_decompress_f16(ctypes.byref(d), *args, T, _stream(stream)))
+
+
+def mla_convert_bf16_to_f16(src: torch.Tensor, dst: torch.Tensor, stream=None):
+    """dst = fp16(src), elementwise (weight preparation, e.g. w_o)."""
+    if src.shape != dst.shape:
+        raise ValueError("src and dst must have the same shape")
+    st = load_library().mla_convert_bf16_to_f16(_need(src, "src", torch.bfloat16), _need(dst, "dst", torch.float16),
+                                                src.numel(), _stream(stream))
+    _check("mla_convert_bf16_to_f16", st)
 
 
 def mla_output_project(o: torch.Tensor, w_o: torch.Tensor, u: torch.Tensor, scale=None, stream=None):
-    """u [T, D] fp32 = o [T, H, 128] bf16 flattened, times w_o [H, 128, D] bf16."""
+    """u [T, D] fp32 = o [T, H, 128] fp16 flattened, times w_o [H, 128, D] fp16."""
     T, H = o.shape[0], o.shape[1]
     D = w_o.shape[2]
     d = make_dims(H, scale)
-    args = (_need(o, "o", torch.bfloat16, (T, H, V_HEAD)), _need(w_o, "w_o", torch.bfloat16, (H, V_HEAD, D)),
+    args = (_need(o, "o", torch.float16, (T, H, V_HEAD)), _need(w_o, "w_o", torch.float16, (H, V_HEAD, D)),
             _need(u, "u", torch.float32, (T, D)))
     _check("mla_output_project", load_library().mla_output_project(ctypes.byref(d), *args, T, D, _stream(stream)))
 

@@ -170,7 +170,7 @@ int decode_common(const mla_dims* dims, const void* q_lat, const void* q_pe, con
 }
 
 int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32_t T, int K, int N, bool f32,
-              void* stream, bool out_bf16 = false) {
+              void* stream, bool out_f16 = false) {
   int s = check_dims(dims);
   if (s != MLA_OK) return s;
   s = check_ptrs({a, w, c});
@@ -178,7 +178,7 @@ int head_gemm(const mla_dims* dims, const void* a, const void* w, void* c, int32
   if (T < 1) return MLA_ERR_INVALID_ARG;
   int* err = nullptr;
   if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
-  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, (f32 || out_bf16) ? 1 : 0, out_bf16 ? 1 : 0};
+  HeadGemmArgs g = {a, w, c, T, dims->n_head, K, N, f32 ? 1 : 0, (f32 || out_f16) ? 1 : 0, out_f16 ? 1 : 0};
   return to_status(launch_head_gemm_tc(g, err, kDefaultWaitUs, static_cast<cudaStream_t>(stream)));
 }
 
@@ -199,8 +199,8 @@ int mla_late_decompress(const mla_dims* dims, const void* o_lat, const void* wv_
   return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, true, stream);
 }
 
-int mla_late_decompress_bf16(const mla_dims* dims, const void* o_lat, const void* wv_b, void* o, int32_t T,
-                             void* stream) {
+int mla_late_decompress_f16(const mla_dims* dims, const void* o_lat, const void* wv_b, void* o, int32_t T,
+                            void* stream) {
   return head_gemm(dims, o_lat, wv_b, o, T, kLatent, kVHead, false, stream, true);
 }
 
@@ -316,6 +316,15 @@ int mla_attn_decode_q8_0(const mla_dims* dims, const void* q_lat, const void* q_
                          int32_t B, int32_t max_len, void* workspace, size_t ws_bytes, void* o_lat, void* stream) {
   return decode_common(dims, q_lat, q_pe, nullptr, kv_q, kv_d, n_rows, seq_start, seq_len, B, max_len, workspace,
                        ws_bytes, o_lat, stream, true);
+}
+
+int mla_convert_bf16_to_f16(const void* src, void* dst, int64_t n, void* stream) {
+  int s = check_ptrs({src, dst});
+  if (s != MLA_OK) return s;
+  if (n < 1 || n % 8 != 0) return MLA_ERR_INVALID_ARG;
+  int* err = nullptr;
+  if (error_word(&err) != cudaSuccess) return MLA_ERR_CUDA;
+  return to_status(launch_bf16_to_f16(src, dst, n, err, static_cast<cudaStream_t>(stream)));
 }
 
 int mla_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d, void* stream) {

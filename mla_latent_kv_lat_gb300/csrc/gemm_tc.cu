@@ -41,7 +41,7 @@ struct TcGemmArgs {
   uint32_t wait_us;
 };
 
-template <int K, int N, int NSUB, bool kAbsorb, bool kOutBf16>
+template <int K, int N, int NSUB, bool kAbsorb, bool kOutF16>
 __global__ void __launch_bounds__(kThreads, 1)
     head_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                         TcGemmArgs g) {
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(w_full);
     }
     bool ok = true;
-    float amax = 0.f;                            // absorb: |q_lat| before its fp16 rounding
+    float amax = 0.f;                            // |q_lat| or |o| before its fp16 rounding
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int tt = grp + i * G;
       const int row = tt * 128 + q * 32 + lane;
@@ -189,15 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o.w = pack_f16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
                 dst[v] = o;
               }
-            } else if constexpr (kOutBf16) {
+            } else if constexpr (kOutF16) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.c) + base);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) amax = f32_absmax(amax, __uint_as_float(r[e]));
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                o.x = pack_f16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                o.y = pack_f16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                o.z = pack_f16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                o.w = pack_f16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
                 dst[v] = o;
               }
             } else {
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&acc_empty[slot]);
       }
     }
-    if (kAbsorb && f32_overflows_f16(amax)) record_error(g.err, MLA_ERR_RANGE);
+    if ((kAbsorb || kOutF16) && f32_overflows_f16(amax)) record_error(g.err, MLA_ERR_RANGE);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -269,7 +271,7 @@ int device_sm_count() {
   return cached[dev];
 }
 
-template <int K, int N, int NSUB, bool kAbsorb, bool kOutBf16>
+template <int K, int N, int NSUB, bool kAbsorb, bool kOutF16>
 static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream) {
   using C = GemmCfg<K, N, NSUB>;
   CUtensorMap tmA, tmW;
@@ -294,7 +296,7 @@ static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, 
   int G = sms / g.H;
   if (G < 1) G = 1;
   if (G > a.tiles) G = a.tiles;
-  auto kern = head_gemm_tc_kernel<K, N, NSUB, kAbsorb, kOutBf16>;
+  auto kern = head_gemm_tc_kernel<K, N, NSUB, kAbsorb, kOutF16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<dim3(g.H, G), kThreads, C::SMEM, stream>>>(tmA, tmW, a);
@@ -302,11 +304,11 @@ static cudaError_t launch_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, 
 }
 
 cudaError_t launch_head_gemm_tc(const HeadGemmArgs& g, int* err, uint32_t wait_us, cudaStream_t stream) {
-  if (g.K == kNope && g.N == kLatent && !g.out_f32 && !g.a_f16 && !g.out_bf16)
+  if (g.K == kNope && g.N == kLatent && !g.out_f32 && !g.a_f16 && !g.out_f16)
     return launch_tc<kNope, kLatent, 256, true, false>(g, err, wait_us, stream);
-  if (g.K == kLatent && g.N == kVHead && g.out_f32 && g.a_f16 && !g.out_bf16)
+  if (g.K == kLatent && g.N == kVHead && g.out_f32 && g.a_f16 && !g.out_f16)
     return launch_tc<kLatent, kVHead, 128, false, false>(g, err, wait_us, stream);
-  if (g.K == kLatent && g.N == kVHead && !g.out_f32 && g.a_f16 && g.out_bf16)
+  if (g.K == kLatent && g.N == kVHead && !g.out_f32 && g.a_f16 && g.out_f16)
     return launch_tc<kLatent, kVHead, 128, false, true>(g, err, wait_us, stream);
   return cudaErrorInvalidValue;
 }

@@ -38,16 +38,16 @@ struct CombineArgs {
 };
 
 // C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: bf16 A, K=128, N=512,
-// fp16 out; late decompression: fp16 A, K=512, N=128, fp32 or bf16 out).
+// fp16 out; late decompression: fp16 A, K=512, N=128, fp32 or fp16 out).
 // W is bf16.
 struct HeadGemmArgs {
   const void* a;            // bf16 or fp16 [T][H][K]
   const void* w;            // bf16 [H][K][N]
-  void* c;                  // fp16, fp32 or bf16 [T][H][N]
+  void* c;                  // fp16 or fp32 [T][H][N]
   int T, H, K, N;
   int out_f32;
   int a_f16;
-  int out_bf16;
+  int out_f16;
 };
 
 // Arguments of the tensor-core latent attention (prefill or decode partials).
@@ -121,10 +121,12 @@ struct PpArgs {
 size_t pp_workspace_bytes(int H, int32_t T, int32_t q_pos0, int hc, bool q8);
 cudaError_t launch_pp_prefill(const PpArgs& p, cudaStream_t stream);
 
-// u[M][N] (fp32) = a[M][K] (bf16) . w_o[K][N] (bf16); K a multiple of 64, N of 64.
+// u[M][N] (fp32) = a[M][K] (fp16) . w_o[K][N] (fp16); K a multiple of 64, N of 64.
 cudaError_t launch_wo_gemm_tc(const void* a, const void* w_o, float* u, int M, int K, int N, int* err,
                               uint32_t wait_us, cudaStream_t stream);
 int device_sm_count();
+// dst[i] = fp16(src[i]) for n bf16 values (records MLA_ERR_RANGE past fp16).
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, int* err, cudaStream_t stream);
 cudaError_t launch_quantize_q8_0(const void* kv, int8_t* kv_q, uint16_t* kv_d, int64_t n, int64_t ld_d,
                                  cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(uint32_t wait_us, int* err, cudaStream_t stream);

@@ -243,6 +243,13 @@ unsigned stage_blocks(int64_t n_units) {
 }
 }  // namespace
 
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, int* err, cudaStream_t stream) {
+  const int64_t n_units = n / 8;
+  cache_bf16_to_f16_kernel<<<stage_blocks(n_units), 256, 0, stream>>>(static_cast<const uint4*>(src),
+                                                                       static_cast<uint4*>(dst), n_units, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_stage_cache_f16(const void* kv, const int8_t* kv_q, const uint16_t* kv_d, int64_t ld_d,
                                    int64_t rows, void* out, int* err, cudaStream_t stream) {
   if (kv != nullptr) {

@@ -10,7 +10,7 @@
 // 16 row tiles of A and 10 column tiles of B, ~140 MB, which L2 holds.  Per tile, K moves
 // in 64-wide steps through a 4-stage TMA ring (A: 128 x 64, K-major; B: 64 x
 // 256, N-major, four 64-column boxes), 128-byte swizzled, on tcgen05 MMAs
-// (M = 128, N = 256, K = 16, bf16 x bf16 -> fp32) into one of two TMEM
+// (M = 128, N = 256, K = 16, fp16 x fp16 -> fp32) into one of two TMEM
 // accumulators, so the epilogue of one tile overlaps the MMAs of the next.
 // Warp 0 issues the copies, warp 1 the MMAs, warps 2-5 drain the accumulators
 // (one TMEM lane quadrant each) through a shared-memory slice, so that each
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // whole warp, converged; one elected lane issues (see mma_ss_warp)
-    constexpr uint32_t idesc = tc::idesc_f16(kBM, kBN, true, false, true);
+    constexpr uint32_t idesc = tc::idesc_f16(kBM, kBN, false, false, true);   // fp16 x fp16
     bool ok = true;
     int u = 0, i = 0;
     for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
@@ -192,11 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_wo_gemm_tc(const void* a, const void* w_o, float* u, int M, int K, int N, int* err,
                               uint32_t wait_us, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
-  // A = o [M][K] bf16 (K-major): 64 x 128 boxes; B = w_o [K][N] bf16 (N-major): 64 x 64 boxes.
-  cudaError_t e = make_tmap_3d(&tmA, a, true, static_cast<uint64_t>(K), static_cast<uint64_t>(M), 1,
+  // A = o [M][K] fp16 (K-major): 64 x 128 boxes; B = w_o [K][N] fp16 (N-major): 64 x 64 boxes.
+  cudaError_t e = make_tmap_3d(&tmA, a, false, static_cast<uint64_t>(K), static_cast<uint64_t>(M), 1,
                                static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(K) * M * 2, kBK, kBM, 1);
   if (e != cudaSuccess) return e;
-  e = make_tmap_3d(&tmB, w_o, true, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 1,
+  e = make_tmap_3d(&tmB, w_o, false, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 1,
                    static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * K * 2, 64, kBK, 1);
   if (e != cudaSuccess) return e;
   WoArgs g;

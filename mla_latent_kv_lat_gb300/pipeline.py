@@ -59,12 +59,12 @@ def mla_prefill(q_nope, q_pe, wk_b, wv_b, q_pos0: int, *, kv=None, kv_q=None, kv
 
 @dataclass
 class ProjectBuffers:
-    o16: torch.Tensor        # bf16 [T, H, 128]: late decompression's output for the projection
+    o16: torch.Tensor        # fp16 [T, H, 128]: late decompression's output for the projection
     u: torch.Tensor          # fp32 [T, D]
 
 
 def project_buffers(T: int, H: int, D: int, device="cuda") -> ProjectBuffers:
-    return ProjectBuffers(torch.empty(T, H, B.V_HEAD, dtype=torch.bfloat16, device=device),
+    return ProjectBuffers(torch.empty(T, H, B.V_HEAD, dtype=torch.float16, device=device),
                           torch.empty(T, D, dtype=torch.float32, device=device))
 
 
@@ -72,7 +72,8 @@ def mla_prefill_projected(q_nope, q_pe, wk_b, wv_b, w_o, q_pos0: int, *, kv=None
                           bufs: Optional[PrefillBuffers] = None, pbufs: Optional[ProjectBuffers] = None,
                           scale=None, stream=None):
     """The path followed by the output projection: absorb -> latent attention ->
-    late decompression (bf16 o) -> u = o . w_o.  Returns (bufs, pbufs)."""
+    late decompression (fp16 o) -> u = o . w_o, with w_o the fp16 weight
+    (mla_convert_bf16_to_f16 of the model's bf16 w_o, once).  Returns (bufs, pbufs)."""
     T, H = q_nope.shape[0], q_nope.shape[1]
     if bufs is None:
         bufs = prefill_buffers(T, H, q_nope.device, n_kv=(kv if kv is not None else kv_q).shape[0])
@@ -85,7 +86,7 @@ def mla_prefill_projected(q_nope, q_pe, wk_b, wv_b, w_o, q_pos0: int, *, kv=None
     else:
         B.mla_attn_prefill_q8_0(bufs.q_lat, q_pe, kv_q, kv_d, q_pos0, bufs.o_lat, bufs.lse, scale=scale,
                                 stream=stream, workspace=bufs.workspace)
-    B.mla_late_decompress_bf16(bufs.o_lat, wv_b, pbufs.o16, scale=scale, stream=stream)
+    B.mla_late_decompress_f16(bufs.o_lat, wv_b, pbufs.o16, scale=scale, stream=stream)
     B.mla_output_project(pbufs.o16, w_o, pbufs.u, scale=scale, stream=stream)
     return bufs, pbufs
 

@@ -14,6 +14,8 @@ from mla_latent_kv_lat_gb300 import workloads as W
 from oracle import mla_oracle as O
 from tests.gpu_util import TOL_BF16, TOL_Q8, Dev, assert_tol, bf16_dev, f16_dev
 
+MLA_ERR_RANGE = -7
+
 pytestmark = pytest.mark.gpu
 
 
@@ -33,34 +35,55 @@ def _lib():
 @pytest.mark.parametrize("H,T,D", [(16, 1, 64), (16, 77, 2048), (32, 300, 320), (128, 257, 7168), (48, 128, 512)])
 def test_output_project_matches_oracle(H, T, D):
     rng = np.random.default_rng(H * 1000 + T)
-    o = W.normal_bf16(rng, (T, H, 128), 0.5)
-    w_o = W.make_wo(H, D, seed=T)
+    o = W.normal_f16(rng, (T, H, 128), 0.5)
+    w_o = W.make_wo(H, D, seed=T).astype(np.float16).astype(np.float32)
     u = torch.full((T, D), float("nan"), dtype=torch.float32, device="cuda")
-    mla.mla_output_project(bf16_dev(o), bf16_dev(w_o), u)
+    mla.mla_output_project(f16_dev(o), f16_dev(w_o), u)
     got = u.cpu().numpy().astype(np.float64)
     ref = O.output_projection(o, w_o)
-    # fp32 accumulation of H*128 exact bf16 x bf16 products
+    # fp32 accumulation of H*128 exact fp16 x fp16 products
     assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(ref)) * np.sqrt(H / 16) + 1e-7
     assert mla.mla_get_device_error() == 0
 
 
-def test_late_decompress_bf16_is_the_rounded_fp32_result():
+def test_late_decompress_f16_is_the_rounded_fp32_result():
     rng = np.random.default_rng(21)
     T, H = 300, 32
     o_lat = f16_dev(W.normal_f16(rng, (T, H, 512), 0.3))
     wv_b = bf16_dev(W.normal_bf16(rng, (H, 512, 128), 1 / np.sqrt(512)))
     o32 = torch.empty(T, H, 128, dtype=torch.float32, device="cuda")
-    o16 = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    o16 = torch.empty(T, H, 128, dtype=torch.float16, device="cuda")
     mla.mla_late_decompress(o_lat, wv_b, o32)
-    mla.mla_late_decompress_bf16(o_lat, wv_b, o16)
-    assert torch.equal(o16, o32.to(torch.bfloat16))     # the same sums, rounded once (nearest even)
+    mla.mla_late_decompress_f16(o_lat, wv_b, o16)
+    assert torch.equal(o16, o32.to(torch.float16))      # the same sums, rounded once (nearest even)
     assert mla.mla_get_device_error() == 0
+
+
+def test_convert_bf16_to_f16_is_exact_and_reports_range():
+    rng = np.random.default_rng(22)
+    src = bf16_dev(W.normal_bf16(rng, (64, 1000), 0.02))
+    src[3, 5] = 0.0
+    src[7, 9] = -1.0e-7                              # lands in fp16's subnormal range
+    dst = torch.full(src.shape, float("nan"), dtype=torch.float16, device="cuda")
+    mla.mla_convert_bf16_to_f16(src, dst)
+    assert torch.equal(dst, src.to(torch.float16))
+    assert mla.mla_get_device_error() == 0
+    src[60, 999] = 1.0e5                             # past fp16's 65504
+    mla.mla_convert_bf16_to_f16(src, dst)
+    assert mla.mla_get_device_error() == MLA_ERR_RANGE
+
+
+def _w_o_f16(w_o: np.ndarray) -> torch.Tensor:
+    """The model's bf16 w_o converted once to the fp16 the projection takes."""
+    w16 = torch.empty(w_o.shape, dtype=torch.float16, device="cuda")
+    mla.mla_convert_bf16_to_f16(bf16_dev(w_o), w16)
+    return w16
 
 
 def _projected_chain(x, rows=None):
     w_o = W.make_wo(x.wl.n_head, x.wl.hidden)
     d = Dev(x)
-    bufs, pb = mla.mla_prefill_projected(d.q_nope, d.q_pe, d.wk_b, d.wv_b, bf16_dev(w_o), x.wl.q_pos0, kv=d.kv)
+    bufs, pb = mla.mla_prefill_projected(d.q_nope, d.q_pe, d.wk_b, d.wv_b, _w_o_f16(w_o), x.wl.q_pos0, kv=d.kv)
     torch.cuda.synchronize()
     assert mla.mla_get_device_error() == 0
     sel = np.arange(x.wl.T) if rows is None else rows
