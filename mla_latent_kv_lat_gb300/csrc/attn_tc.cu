@@ -31,11 +31,11 @@
 //     once: seven producer warps load the latent tiles with software-pipelined
 //     16-byte loads, convert them to fp16 (bf16: exact; q8_0: fp16 scale x
 //     int8 code) and store them swizzled; the bf16 RoPE part arrives by TMA.
-//   * Roles per CTA: warps 0-7 softmax / exchange / epilogue (two threads per
-//     row, 32 keys of each 64-key tile each); then the loader (prefill: one
-//     TMA warp; decode: seven producer warps); the last warp issues the MMAs.  Every mbarrier wait is bounded; the two softmax warps that share
-//     rows meet at a named barrier once per tile, and a warp whose wait gave up
-//     keeps meeting its partner (doing no other work) so that neither can hang.
+//   * Roles per CTA: warps 0-7 softmax / exchange (two threads per row, lanes
+//     l and l + 16 of one warp, 32 keys of each 64-key tile each, so the row
+//     maximum is one shuffle); then the epilogue warps, the loader (prefill:
+//     one TMA warp; decode: TMA and converter warps, or seven q8_0 producer
+//     warps); the last warp(s) issue the MMAs.  Every mbarrier wait is bounded.
 #include <string.h>
 
 #include "kernels.cuh"
@@ -64,14 +64,14 @@ constexpr int kOffRope = kOffLat + kLatStages * kLatStage;
 constexpr int kOffP = kOffRope + kRopeStages * kRopeChunk;
 constexpr int kOffX = kOffP + 2 * kPBytes;
 constexpr int kOffAux = kOffX + 2 * kXBytes;
-// Two softmax threads per query row, each taking 32 keys of every tile (the
-// code is written for kTpr threads per row; one and four measured slower).
+// Two softmax threads per query row, each taking 32 keys of every tile: lanes
+// l and l + 16 of one warp, which reads its 16 TMEM lanes in two column
+// halves (tcgen05.ld 16x32bx2).  (One thread per row, or four over two warps,
+// measured slower; two in two warps, meeting at a named barrier for the row
+// maximum, 4-5% slower on prefill.)
 constexpr int kTpr = 2;
-constexpr int kMaxTpr = 2, kMaxSoftmaxWarps = 4 * kMaxTpr;
-// row maxima [tile parity][thread of row][row], row sums [thread of row][row],
-// the row sums handed to the epilogue warps [item parity][row], failure
-// flags [tile parity][warp]
-constexpr int kAuxBytes = (2 * kMaxTpr * kRows + kMaxTpr * kRows + 2 * kRows) * 4 + 2 * kMaxSoftmaxWarps * 4;
+// the row sums handed to the epilogue warps [item parity][row]
+constexpr int kAuxBytes = 2 * kRows * 4;
 // Epilogue warps' output staging: 2 KB per warp (32 rows x 64 B), so that the
 // global stores leave as 64-byte row pieces, not 16-byte pieces of 32 rows.
 constexpr int kStgBytes = 4 * 2048;
@@ -124,6 +124,15 @@ constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 256 in fp16
 
+// Where a decode cluster's tile range starts: computed once per CTA, by one
+// warp during setup (a lane per sequence, so the sequence table costs two
+// round trips however many roles walk it), and read by every role.
+struct DecodeStart {
+  int64_t lo, hi;   // the cluster's tile range [lo, hi) in the run of all sequences' tiles
+  int64_t S;        // first tile of sequence b
+  int b;            // the first sequence that ends after lo (n_seq: none)
+};
+
 struct Bars {
   uint64_t lat_full[kLatStages];
   uint64_t lat_tma[kLatStages];   // bf16 decode: the TMA tile has landed (before conversion)
@@ -142,6 +151,7 @@ struct Bars {
   uint64_t o_ready;   // commit per item (prefill): its last P.V has completed
   uint64_t l_ready[2];   // arrival per item (prefill), by item parity: row sums in aux
   uint32_t tmem;
+  DecodeStart ds;        // decode: this cluster's start (written in setup)
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 static_assert(kSmem <= 232448, "shared memory");
@@ -277,11 +287,47 @@ MLA_DEVINL Item prefill_item(const AttnTcArgs& a, int idx) {
 template <bool kDecode>
 struct ItemIter;
 
+// Whole warp.  Invalid sequences count 0 tiles (they are skipped).
+MLA_DEVINL DecodeStart decode_start(const AttnTcArgs& a, int c, int g, int lane) {
+  auto tiles = [&](int q) -> int64_t {
+    return q < a.n_seq ? decode_seq_tiles(decode_valid_len(a.seq_start, a.seq_len, q, a.max_len, a.n_rows)) : 0;
+  };
+  int64_t T = 0;
+  for (int q0 = 0; q0 < a.n_seq; q0 += 32) T += tiles(q0 + lane);
+  T = warp_sum_i64(T);
+  const int64_t lo = decode_cluster_lo(T, g, c), hi = decode_cluster_lo(T, g, c + 1);
+  int b = a.n_seq;
+  int64_t S = T, run = 0;
+  for (int q0 = 0; q0 < a.n_seq; q0 += 32) {
+    const int64_t t = tiles(q0 + lane);
+    int64_t incl = t;                         // inclusive scan over the lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, q0 + lane < a.n_seq && run + incl > lo);
+    if (hit != 0u) {
+      const int f = __ffs(hit) - 1;
+      b = q0 + f;
+      S = run + __shfl_sync(0xffffffffu, incl - t, f);
+      break;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  DecodeStart out;
+  out.lo = lo;
+  out.hi = hi;
+  out.S = S;
+  out.b = b;
+  return out;
+}
+
 template <>
 struct ItemIter<false> {
   const AttnTcArgs* a;
   int c, g, r;
-  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters, const DecodeStart*) {
     a = &args; c = cluster; g = clusters; r = 0;
   }
   MLA_DEVINL bool next(Item& it) {
@@ -299,57 +345,12 @@ struct ItemIter<false> {
 template <>
 struct ItemIter<true> {
   const AttnTcArgs* a;
-  int c, g;
+  int c;
   int b;                       // next sequence
   int64_t lo, hi, S;           // cluster tile range, first tile of sequence b
-  // Tiles of sequences [q0, q0 + 8) (invalid ones count 0), and with `stop`
-  // the number of them that end at or before tile `stop` given the run
-  // reaches `base` at q0.  The loads of all eight are in flight at once: the
-  // sequence table is read by every role of every CTA at the start.
-  MLA_DEVINL void batch(int q0, int32_t (&tiles)[8]) const {
-    int32_t len[8];
-    int64_t st[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = q0 + j < a->n_seq;
-      len[j] = in ? a->seq_len[q0 + j] : 0;
-      st[j] = in ? a->seq_start[q0 + j] : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool ok = len[j] >= 1 && len[j] <= a->max_len && st[j] >= 0 && st[j] <= a->n_rows - len[j];
-      tiles[j] = ok ? static_cast<int32_t>(decode_seq_tiles(len[j])) : 0;     // invalid: skipped
-    }
-  }
-  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
-    a = &args; c = cluster; g = clusters;
-    int64_t T = 0;
-    for (int q0 = 0; q0 < a->n_seq; q0 += 8) {
-      int32_t t[8];
-      batch(q0, t);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) T += t[j];
-    }
-    lo = decode_cluster_lo(T, g, c);
-    hi = decode_cluster_lo(T, g, c + 1);
-    // skip the sequences that end before this cluster's range
-    b = 0;
-    S = 0;
-    for (int q0 = 0; q0 < a->n_seq; q0 += 8) {
-      int32_t t[8];
-      batch(q0, t);
-      bool stop = false;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (!stop && S + t[j] <= lo && q0 + j < a->n_seq) {
-          S += t[j];
-          b = q0 + j + 1;
-        } else {
-          stop = true;
-        }
-      }
-      if (stop) break;
-    }
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int, const DecodeStart* ds) {
+    a = &args; c = cluster;
+    lo = ds->lo; hi = ds->hi; S = ds->S; b = ds->b;
   }
   MLA_DEVINL bool next(Item& it) {
     while (b < a->n_seq && S < hi) {
@@ -387,8 +388,8 @@ struct TileCursor {
       t = 0;
     }
   }
-  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters) {
-    iter.init(args, cluster, clusters);
+  MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int clusters, const DecodeStart* ds) {
+    iter.init(args, cluster, clusters, ds);
     t = 0;
     more = iter.next(it);
     skip_empty();
@@ -435,19 +436,20 @@ MLA_DEVINL void store_rows64(uint8_t* stg, int lane, const uint4 (&w)[4], uint8_
   __syncwarp();
 }
 
-// L2 prefetch of one decode tile's cache rows (the rows of both CTAs' parts).
-constexpr int kPrefetchTiles = 8;
-template <bool kDecode>
-MLA_DEVINL void prefetch_tile_rows(const AttnTcArgs& a, const TileCursor<kDecode>& c) {
-  const int64_t row0 = c.it.key_base + static_cast<int64_t>(c.t) * kBK;
-  const int64_t rows = min(static_cast<int64_t>(kBK), a.n_rows - row0);
-  if (rows <= 0) return;
-  if (a.kv != nullptr) {
+// bf16 decode: before waiting for tile u's stage, each CTA asks for the whole
+// rows of tile u (both CTAs' parts) as one contiguous L2 prefetch, so the
+// rows are on their way while the stage drains.  Measured against the TMA
+// loads alone (B=32 decode): 7% faster; prefetching 1, 2, 4 or 8 tiles ahead
+// instead, with or without an evict-last hint, gave back most or all of it.
+MLA_DEVINL void prefetch_rows_l2(const AttnTcArgs& a, int64_t row0, int64_t nrows) {
+  const int64_t rows = min(nrows, a.n_rows - row0);
+  if (rows > 0)
     tc::prefetch_l2(static_cast<const uint16_t*>(a.kv) + row0 * kRow, static_cast<uint32_t>(rows * kRow * 2));
-  } else {
-    tc::prefetch_l2(a.kv_q + row0 * kRow, static_cast<uint32_t>(rows * kRow));
-  }
 }
+
+// q8_0 decode: L2 prefetch of the rows kPrefetchTiles tiles ahead of the
+// producers' loads.
+constexpr int kPrefetchTiles = 8;
 
 // q8_0 tiles ahead, by one warp (lane = pt < 32): the codes as one bulk L2
 // prefetch, and the scales of the tile's rows in each of the 18 scale blocks
@@ -473,7 +475,7 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   using P = Producer<kQ8, kRope>;
   const bool uses_rope = kRope || tma_rope;
   TileCursor<true> cur;
-  cur.init(a, first, stride);
+  cur.init(a, first, stride, &B.ds);
   if (!cur.valid()) return;
   // One thread keeps the rows of the tiles kPrefetchTiles ahead on their way into L2.
   TileCursor<true> ahead = cur;
@@ -560,10 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
   uint8_t* sP = sm + kOffP;
   uint8_t* sX = sm + kOffX;
   uint8_t* sStg = sm + kOffStg;
-  float* aux_m = reinterpret_cast<float*>(sm + kOffAux);        // [2][kTpr][128] row maxima
-  float* aux_l = aux_m + 2 * kMaxTpr * kRows;                   // [kTpr][128] row sums
-  float* aux_lrow = aux_l + kMaxTpr * kRows;                    // [2][128] row sums for the epilogue warps
-  int* aux_fail = reinterpret_cast<int*>(aux_lrow + 2 * kRows); // [2][8] per-warp failure flags
+  float* aux_lrow = reinterpret_cast<float*>(sm + kOffAux);     // [2][128] row sums for the epilogue warps
   Bars& B = *reinterpret_cast<Bars*>(sm + kOffBar);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
@@ -604,6 +603,23 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     tc::tmem_alloc(&B.tmem, 512);
     tc::tmem_relinquish();
   }
+  if constexpr (kDecode) {
+    if (warp == 1) {
+      const DecodeStart ds = decode_start(a, first, stride, lane);
+      if (lane == 0) {
+        B.ds = ds;
+        // The first item's queries on their way into L2 (its Q load is the
+        // longest step before the first tile).
+        if (ds.b < a.n_seq) {
+          const int64_t r0 = static_cast<int64_t>(ds.b) * a.n_head;
+          if (rank == 0)
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_lat) + r0 * kLatent, static_cast<uint32_t>(a.n_head) * kLatent * 2);
+          else
+            tc::prefetch_l2(static_cast<const uint16_t*>(a.q_pe) + r0 * kRope, static_cast<uint32_t>(a.n_head) * kRope * 2);
+        }
+      }
+    }
+  }
   tc::fence_before_sync();
   tc::cluster_sync();                 // peer barriers initialised before any remote arrival
   tc::fence_after_sync();
@@ -614,21 +630,22 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 
   if (warp < kSoftmaxWarps) {
     // ======================= softmax / exchange / epilogue =====================
-    // kTpr threads share a query row (one per warp of the same lane quadrant):
-    // thread hh takes keys [kKpt*hh, kKpt*hh + kKpt) of every tile and output
-    // columns [kOpt*hh, kOpt*hh + kOpt) of this CTA's half.
+    // Warp w serves the 16 TMEM lanes (query rows) 32 (w % 4) + 16 (w / 4) ..
+    // +15; lanes l and l + 16 share row l % 16: thread hh = l / 16 takes keys
+    // [kKpt*hh, kKpt*hh + kKpt) of every tile and output columns
+    // [kOpt*hh, kOpt*hh + kOpt) of this CTA's half.
+    static_assert(kTpr == 2, "two threads per row: lanes l and l + 16 of one warp");
     const int q4 = warp & 3;                    // TMEM lane quadrant
-    const int hh = warp >> 2;                   // which share of the row
-    const int i = q4 * 32 + lane;               // query row == TMEM lane
-    const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
+    const int hh = lane >> 4;                   // which half of the row's keys and output columns
+    const int i = q4 * 32 + (warp >> 2) * 16 + (lane & 15);   // query row == TMEM lane
+    const uint32_t lanes = static_cast<uint32_t>(q4 * 32 + (warp >> 2) * 16) << 16;   // the warp's 16 lanes
     const float c2 = a.scale_log2;              // raw score -> log2 units
     const uint32_t peer_x = tc::mapa(smem_u32(sX), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(&B.x_full[0]), peer);
     const uint32_t peer_xempty = tc::mapa(smem_u32(&B.x_empty[0]), peer);
-    const int bar_id = 1 + q4;                  // named barrier of the kTpr warps sharing these rows
-    // A wait that gave up makes the warp "dead": it skips every later wait,
-    // tensor-memory access and arrival, but still meets its partner warps at
-    // every named barrier, so no warp of a row group can be left waiting.
+    // A wait that gave up makes the warp "dead" (every wait is warp-wide, so
+    // the whole warp): it skips every later wait, tensor-memory access and
+    // arrival.
     bool dead = false;
     auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
       if (!dead) dead = !wait_all(bar, parity, a);
@@ -643,7 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (dead) return;
       tc::fence_after_sync();
       uint32_t r[kKpt];
-      tc::tmem_ld<kKpt>(tmem + lanes + kTmS + sb * 64 + kKpt * hh, r);
+      tc::tmem_ld16x2<kKpt>(tmem + lanes + kTmS + sb * 64, r);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       mbar_arrive(&B.s_free[sb]);
@@ -666,26 +683,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (threadIdx.x == 0) mbar_arrive_expect_tx(&B.x_full[sb], kXBytes);
     };
 
-    // Meet the other warps of this row group: publish `val` (in slot
-    // base[hh][row]) and this warp's state; the caller then reads the group's
-    // values from base.
-    auto group_meet = [&](float* base, float val, int phase) {
-      base[hh * kRows + i] = val;
-      if constexpr (kTpr == 1) return;           // the row has one thread: nothing to meet
-      if (lane == 0) aux_fail[(phase & 1) * kMaxSoftmaxWarps + warp] = dead ? 1 : 0;
-      tc::named_bar_sync(bar_id, kTpr * 32);
-#pragma unroll
-      for (int g = 0; g < kTpr; ++g)
-        if (aux_fail[(phase & 1) * kMaxSoftmaxWarps + q4 + 4 * g] != 0) dead = true;
-    };
-
     uint32_t own[kKpt / 2], nxt[kKpt / 2];
     uint32_t qrun = 0;                          // q_pe converted here (q8_0 decode): fp16 range check
     bool score_range = false;                   // a row maximum became infinite or NaN
     int u0 = 0;                                 // this item's first tile, counted across items
     int k = 0;                                  // items done
     ItemIter<kDecode> items;
-    items.init(a, first, stride);
+    items.init(a, first, stride, &B.ds);
     Item it;
 #pragma unroll 1
     while (items.next(it)) {
@@ -720,7 +724,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         for (int v = 0; v < 4 / kTpr; ++v)      // this CTA's 32 RoPE dims: units 4 rank .. 4 rank + 3
           qpe[v] = rvalid ? __ldg(qp + 4 * rank + (4 / kTpr) * hh + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int c = 0; c < kOpt / 64; ++c) tc::tmem_st32(tmem + lanes + kTmQ + (kOpt / 2) * hh + 32 * c, r[c]);
+        for (int c = 0; c < kOpt / 64; ++c) tc::tmem_st16x2<kOpt / 2>(tmem + lanes + kTmQ + 32 * c, r[c]);
         tc::tmem_st_wait();
         {                                       // RoPE query part -> smem (bf16 as is, or fp16)
 #pragma unroll
@@ -771,11 +775,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
         for (int w = kKpt / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-        float* mslot = aux_m + (u & 1) * kMaxTpr * kRows;
-        group_meet(mslot, mx[0] * c2, u);
-        float mrow = mslot[i];
-#pragma unroll
-        for (int g = 1; g < kTpr; ++g) mrow = fmaxf(mrow, mslot[g * kRows + i]);
+        const float mown = mx[0] * c2;
+        const float mrow = fmaxf(mown, __shfl_xor_sync(0xffffffffu, mown, 16));
         // Lazy rescale: only when the row max grew by more than the threshold (always on the first tile).
         float alpha = 1.f;
         if (mrow > m_run + kRescaleThreshold) {
@@ -804,12 +805,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
 #pragma unroll 1
             for (int c = 0; c < kOpt / 32; ++c) {
               uint32_t o[32];
-              const uint32_t col = tmem + lanes + kTmO + kOpt * hh + 32 * c;
-              tc::tmem_ld32(col, o);
+              const uint32_t col = tmem + lanes + kTmO + 32 * c;
+              tc::tmem_ld16x2<kOpt>(col, o);
               tc::tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tc::tmem_st32(col, o);
+              tc::tmem_st16x2<kOpt>(col, o);
             }
             tc::tmem_st_wait();
           }
@@ -877,10 +878,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if (rvalid && !dead && !(m_run < INFINITY)) score_range = true;
       if constexpr (kEpi) {
         // Prefill: hand the row sums to the epilogue warps and go on.
-        group_meet(aux_l, l_h, u0 + n);
-        float l_row = aux_l[i];                 // the same order in every thread of the row
-#pragma unroll
-        for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
+        const float l_row = l_h + __shfl_xor_sync(0xffffffffu, l_h, 16);   // a + b == b + a: the same in both threads
         if (hh == 0) aux_lrow[(k & 1) * kRows + i] = l_row;
         if (rank == 0 && hh == 0 && rvalid) {
           if constexpr (kDecode) {
@@ -894,17 +892,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       } else {
         // Decode: O / l -> the fp32 partials, with the running max and sum.
         wait_ok(&B.pv_done[(u0 + n - 1) & 1], ((u0 + n - 1) >> 1) & 1);
-        group_meet(aux_l, l_h, u0 + n);
         if (!dead) {
           tc::fence_after_sync();
-          float l_row = aux_l[i];               // the same order in every thread of the row
-#pragma unroll
-          for (int g = 1; g < kTpr; ++g) l_row += aux_l[g * kRows + i];
+          const float l_row = l_h + __shfl_xor_sync(0xffffffffu, l_h, 16);
           const float inv = 1.f / l_row;
 #pragma unroll 1
           for (int c = 0; c < kOpt / 32; ++c) {
             uint32_t o[32];
-            tc::tmem_ld32(tmem + lanes + kTmO + kOpt * hh + 32 * c, o);
+            tc::tmem_ld16x2<kOpt>(tmem + lanes + kTmO + 32 * c, o);
             tc::tmem_ld_wait();
             if (!rvalid) continue;
             const int col = 256 * static_cast<int>(rank) + kOpt * hh + 32 * c;
@@ -1144,7 +1139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       // start).
       const int ct = epi ? 64 + q4 * 32 + lane : (warp - kLoaderWarp - 1) * 32 + lane;
       TileCursor<kDecode> cur;
-      cur.init(a, first, stride);
+      cur.init(a, first, stride, &B.ds);
       // One pass past the last tile writes the last item's output (one call
       // site of the epilogue: the decode kernel is instruction-fetch bound).
 #pragma unroll 1
@@ -1177,30 +1172,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     if constexpr (!kDecode || !kQ8) {
       if (pt == 0) {
         // One thread: each tile's four 64-dim latent chunks of this CTA's half
-        // (and, on rank 0, the RoPE part) by TMA, as soon as the stage is free.
-        // Prefill reads the fp16 staging copy (the tile is ready on arrival);
-        // the bf16 decode reads the cache itself and the tile is converted
-        // before the MMAs may read it.
+        // and its 32 RoPE dims by TMA, as soon as the stage is free.  Prefill
+        // reads the fp16 staging copy (the tile is ready on arrival); the bf16
+        // decode reads the cache itself and the tile is converted before the
+        // MMAs may read it.
         uint64_t* landed = kDecode ? B.lat_tma : B.lat_full;
-        TileCursor<kDecode> cur, ahead;
-        cur.init(a, first, stride);
-        // Decode reads every cache row from HBM once: keep the rows of the
-        // tiles kPrefetchTiles ahead on their way into L2, so that a stage's
-        // TMA, issued only when its previous tile is done, finds them there.
-        if (kDecode) {
-          ahead = cur;
-          for (int d = 0; d < kPrefetchTiles && ahead.valid(); ++d) {
-            if (rank == 0) prefetch_tile_rows(a, ahead);
-            ahead.next();
-          }
-        }
+        TileCursor<kDecode> cur;
+        cur.init(a, first, stride, &B.ds);
         for (int u = 0; cur.valid(); ++u, cur.next()) {
           const int ls = u % kLatStages, rs = u % kRopeStages;
           const int key = static_cast<int>(cur.it.key_base) + cur.t * kBK;
-          if (kDecode && ahead.valid()) {
-            if (rank == 0) prefetch_tile_rows(a, ahead);
-            ahead.next();
-          }
+          if (kDecode) prefetch_rows_l2(a, key, min(kBK, cur.it.kend - cur.t * kBK));
           if (u >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((u / kLatStages) - 1) & 1, a.wait_us, a.err))
             break;
           mbar_arrive_expect_tx(&landed[ls], kLatStage);
@@ -1276,7 +1258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       // three tiles ahead of P.V).
       int u = 0, k = 0;
       ItemIter<kDecode> items;
-      items.init(a, first, stride);
+      items.init(a, first, stride, &B.ds);
       Item it;
       while (ok && items.next(it)) {
         if (warp == kMmaWarp) {
@@ -1300,7 +1282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       // issued after the current item's last P.V.
       int u = 0, k = 0;
       ItemIter<kDecode> items;
-      items.init(a, first, stride);
+      items.init(a, first, stride, &B.ds);
       Item it;
       while (ok && items.next(it)) {
         const int n = it.n_tiles;

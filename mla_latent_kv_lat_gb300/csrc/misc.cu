@@ -102,17 +102,24 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
   }
   const int64_t Eb = Sb + decode_seq_tiles(len_b);
   const int G = c.n_clusters;
+  // The clusters' range starts lo(x) = T x / G, x = 0..G, once per block (a
+  // 64-bit division each: computed on the fly they made this kernel
+  // instruction-bound).
+  extern __shared__ long long s_lo[];
+  for (int x = threadIdx.x; x <= G; x += blockDim.x) s_lo[x] = decode_cluster_lo(T, G, x);
+  __syncthreads();
+  auto lo = [&](int x) { return s_lo[x]; };
   // The first cluster whose range meets [Sb, Eb): ranges are [lo(c), lo(c+1)).
   int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Sb * G / max(T, static_cast<int64_t>(1))));
-  while (c0 > 0 && decode_cluster_lo(T, G, c0) > Sb) --c0;
-  while (c0 + 1 < G && decode_cluster_lo(T, G, c0 + 1) <= Sb) ++c0;
+  while (c0 > 0 && lo(c0) > Sb) --c0;
+  while (c0 + 1 < G && lo(c0 + 1) <= Sb) ++c0;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the attention kernel's partials are complete
   const int h = blockIdx.y * kCombHeads + warp;
   if (h >= c.n_head) return;
   // Pass 1: the largest running max over the pieces (a lane per piece).
   float M = -INFINITY;
-  for (int x = c0 + lane; x < G && decode_cluster_lo(T, G, x) < Eb; x += 32) {
-    if (decode_cluster_lo(T, G, x + 1) <= decode_cluster_lo(T, G, x)) continue;   // empty range
+  for (int x = c0 + lane; x < G && lo(x) < Eb; x += 32) {
+    if (lo(x + 1) <= lo(x)) continue;   // empty range
     M = fmaxf(M, c.ws_ml[2 * ((static_cast<int64_t>(b) + x) * c.n_head + h)]);
   }
   M = warp_max(M);
@@ -122,7 +129,6 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   int cl = c0;
-  auto lo = [&](int x) { return decode_cluster_lo(T, G, x); };
   while (cl < G && lo(cl) < Eb) {
     // the next (up to) four non-empty pieces
     int64_t slot[4];
@@ -177,7 +183,7 @@ cudaError_t launch_combine(const CombineArgs& c, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c.B), static_cast<unsigned>((c.n_head + kCombHeads - 1) / kCombHeads));
   cfg.blockDim = dim3(32 * kCombHeads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(c.n_clusters + 1) * sizeof(long long);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
