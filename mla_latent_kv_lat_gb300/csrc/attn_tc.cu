@@ -70,8 +70,8 @@ constexpr int kOffAux = kOffX + 2 * kXBytes;
 // measured slower; two in two warps, meeting at a named barrier for the row
 // maximum, 4-5% slower on prefill.)
 constexpr int kTpr = 2;
-// the row sums handed to the epilogue warps [item parity][row]
-constexpr int kAuxBytes = 2 * kRows * 4;
+// the row sums handed to the epilogue warps [item % 4][row]
+constexpr int kAuxBytes = 4 * kRows * 4;
 // Epilogue warps' output staging: 2 KB per warp (32 rows x 64 B), so that the
 // global stores leave as 64-byte row pieces, not 16-byte pieces of 32 rows.
 constexpr int kStgBytes = 4 * 2048;
@@ -133,6 +133,13 @@ struct DecodeStart {
   int b;            // the first sequence that ends after lo (n_seq: none)
 };
 
+// Barriers that count arrivals from several warps are deep enough that a warp
+// running ahead cannot arrive for a later use before every warp has arrived for
+// the earlier one.  The softmax warps are coupled only through barriers and
+// may drift a tile or two apart, so: one P barrier per P buffer (a warp stores
+// P of tile u+2 only after P.V(u) has read that buffer, which needed every
+// warp's P of tile u), and four row-sum slots (a warp ends item k+4 only after
+// P.V of item k+2's first tile, which waited for the epilogue of item k+1).
 struct Bars {
   uint64_t lat_full[kLatStages];
   uint64_t lat_tma[kLatStages];   // bf16 decode: the TMA tile has landed (before conversion)
@@ -143,13 +150,13 @@ struct Bars {
   uint64_t s_free[2];
   uint64_t x_full[2];
   uint64_t x_empty[2];
-  uint64_t p_full;
+  uint64_t p_full[2];    // by P buffer: all softmax threads have stored their P of the tile using it
   uint64_t pv_done[2];   // by P buffer: P.V of the tile that used it has completed
   uint64_t q_ready;   // arrival per item: Q of the next item is in TMEM
   uint64_t o_free;    // arrival per item: the epilogue has read O
   uint64_t q_free;    // commit per item (prefill): its last score MMA has completed
   uint64_t o_ready;   // commit per item (prefill): its last P.V has completed
-  uint64_t l_ready[2];   // arrival per item (prefill), by item parity: row sums in aux
+  uint64_t l_ready[4];   // arrival per item (prefill, bf16 decode), by item % 4: row sums in aux
   uint32_t tmem;
   DecodeStart ds;        // decode: this cluster's start (written in setup)
 };
@@ -562,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
   uint8_t* sP = sm + kOffP;
   uint8_t* sX = sm + kOffX;
   uint8_t* sStg = sm + kOffStg;
-  float* aux_lrow = reinterpret_cast<float*>(sm + kOffAux);     // [2][128] row sums for the epilogue warps
+  float* aux_lrow = reinterpret_cast<float*>(sm + kOffAux);     // [4][128] row sums for the epilogue warps
   Bars& B = *reinterpret_cast<Bars*>(sm + kOffBar);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
@@ -588,15 +595,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       mbar_init(&B.x_full[i], 1);
       mbar_init(&B.x_empty[i], kSoftmaxWarps);
     }
-    mbar_init(&B.p_full, kSoftmaxWarps * 32);
+    mbar_init(&B.p_full[0], kSoftmaxWarps * 32);
+    mbar_init(&B.p_full[1], kSoftmaxWarps * 32);
     mbar_init(&B.pv_done[0], 1);
     mbar_init(&B.pv_done[1], 1);
     mbar_init(&B.q_ready, kEpi ? 128 : kSoftmaxWarps * 32);
     mbar_init(&B.o_free, kEpi ? 128 : kSoftmaxWarps * 32);
     mbar_init(&B.q_free, 1);
     mbar_init(&B.o_ready, 1);
-    mbar_init(&B.l_ready[0], kSoftmaxWarps * 32);
-    mbar_init(&B.l_ready[1], kSoftmaxWarps * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&B.l_ready[i], kSoftmaxWarps * 32);
     tc::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -821,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
           st_unit(sP + (u & 1) * kPBytes, i, kUpt * hh + g, make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
         tc::fence_proxy_async();
         tc::fence_before_sync();
-        mbar_arrive(&B.p_full);
+        mbar_arrive(&B.p_full[u & 1]);
         // This warp has long finished reading exchange buffer xb (every value read
         // from it fed the scores above): tell the peer it may refill it.  A relaxed
         // arrival suffices and avoids the ~1.4k-cycle cluster-scope release.
@@ -879,7 +886,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       if constexpr (kEpi) {
         // Prefill: hand the row sums to the epilogue warps and go on.
         const float l_row = l_h + __shfl_xor_sync(0xffffffffu, l_h, 16);   // a + b == b + a: the same in both threads
-        if (hh == 0) aux_lrow[(k & 1) * kRows + i] = l_row;
+        if (hh == 0) aux_lrow[(k & 3) * kRows + i] = l_row;
         if (rank == 0 && hh == 0 && rvalid) {
           if constexpr (kDecode) {
             a.ws_ml[2 * (it.slot0 + i)] = m_run;
@@ -888,7 +895,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
             a.lse[qrow] = (m_run + log2f(l_row)) * kLn2;
           }
         }
-        mbar_arrive(&B.l_ready[k & 1]);
+        mbar_arrive(&B.l_ready[k & 3]);
       } else {
         // Decode: O / l -> the fp32 partials, with the running max and sum.
         wait_ok(&B.pv_done[(u0 + n - 1) & 1], ((u0 + n - 1) >> 1) & 1);
@@ -938,10 +945,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     bool ok = true;
     auto epilogue = [&](const Item& pv, int kk) {
       ok = ok && wait_all(&B.o_ready, kk & 1, a);
-      ok = ok && wait_all(&B.l_ready[kk & 1], (kk >> 1) & 1, a);
+      ok = ok && wait_all(&B.l_ready[kk & 3], (kk >> 2) & 1, a);
       if (!ok) return;
       tc::fence_after_sync();
-      const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
+      const float inv = 1.f / aux_lrow[(kk & 3) * kRows + i];
       // This warp's 32 rows, 32 columns (64 B of fp16) per step, through its staging slice.
       uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(a.o_lat) + (pv.qrow0 + q4 * 32) * kLatent +
                                                 256 * rank);
@@ -1047,10 +1054,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     bool ok = true;
     auto epilogue = [&](const Item& pv, int kk) {
       ok = ok && wait_all(&B.o_ready, kk & 1, a);
-      ok = ok && wait_all(&B.l_ready[kk & 1], (kk >> 1) & 1, a);
+      ok = ok && wait_all(&B.l_ready[kk & 3], (kk >> 2) & 1, a);
       if (!ok) return;
       tc::fence_after_sync();
-      const float inv = 1.f / aux_lrow[(kk & 1) * kRows + i];
+      const float inv = 1.f / aux_lrow[(kk & 3) * kRows + i];
       // fp32 partial of this piece, normalised by its own sum: this warp's 32
       // rows, 16 columns (64 B) per step, through its staging slice.
       uint8_t* dst = reinterpret_cast<uint8_t*>(a.ws_o + (pv.slot0 + q4 * 32) * kLatent + 256 * rank);
@@ -1239,7 +1246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
     // `t0`: first tile of its item (O restarts; the previous item's epilogue
     // must have read O, the k-th arrival on o_free).
     auto issue_pv = [&](int u, bool t0, int k) -> bool {
-      if (!wait_all(&B.p_full, u & 1, a)) return false;
+      if (!wait_all(&B.p_full[u & 1], (u >> 1) & 1, a)) return false;
       if (t0 && k > 0 && !wait_all(&B.o_free, (k - 1) & 1, a)) return false;
       tc::fence_after_sync();
       const uint32_t v0 = smem_u32(sLat + (u % kLatStages) * kLatStage);
