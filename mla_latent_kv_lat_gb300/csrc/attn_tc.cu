@@ -28,9 +28,11 @@
 //     the rows are staged once as fp16 (latent and RoPE parts) before the
 //     kernel, and one thread brings each tile in by TMA, already in the
 //     128-byte-swizzled layout the tensor core reads.  Decode reads each row
-//     once: seven producer warps load the latent tiles with software-pipelined
-//     16-byte loads, convert them to fp16 (bf16: exact; q8_0: fp16 scale x
-//     int8 code) and store them swizzled; the bf16 RoPE part arrives by TMA.
+//     once.  bf16 cache: the tiles arrive by TMA (each CTA first asks L2 for
+//     the tile's whole rows) and six warps convert the latent part to fp16 in
+//     place (exact); the RoPE part is used as bf16.  q8_0 cache: seven producer
+//     warps load codes and scales one tile ahead, dequantise (fp16 scale x
+//     int8 code) and store the fp16 tiles swizzled.
 //   * Roles per CTA: warps 0-7 softmax / exchange (two threads per row, lanes
 //     l and l + 16 of one warp, 32 keys of each 64-key tile each, so the row
 //     maximum is one shuffle); then the epilogue warps, the loader (prefill:
@@ -189,21 +191,17 @@ MLA_DEVINL uint4 bf16x8_to_f16x8(uint4 v) {
 
 
 // ---------------------------------------------------------------------------
-// Producer: one 64-key tile of this CTA's cache part.
-//   bf16 cache: the 256 latent dims (32 units of 8 values per key); the RoPE
-//               part comes by TMA.
-//   q8_0 cache: the 256 latent dims (16 units of 16 codes per key) plus this
-//               CTA's 32 RoPE dims (2 units), dequantised to fp16.
+// q8_0 decode producer: one 64-key tile of this CTA's cache part, the 256
+// latent dims (16 units of 16 codes per key) plus this CTA's 32 RoPE dims (2
+// units), dequantised to fp16 (fp16 scale x int8 code).
 // ---------------------------------------------------------------------------
-template <bool kQ8, bool kRope>
-struct Producer {
-  static constexpr int LAT_UPK = kQ8 ? 16 : 32;
-  static constexpr int UPK = LAT_UPK + ((kQ8 && kRope) ? 2 : 0);
+struct Q8Producer {
+  static constexpr int UPK = 16 + 2;
   static constexpr int NUNITS = kBK * UPK;
   static constexpr int NU = (NUNITS + kProducerThreads - 1) / kProducerThreads;
   uint4 v[NU];
-  uint32_t d[kQ8 ? NU : 1];   // raw fp16 scale bits: converted at store time, so no
-                               // instruction waits on the load before then
+  uint32_t d[NU];   // raw fp16 scale bits: converted at store time, so no
+                    // instruction waits on the load before then
 
   MLA_DEVINL void load(const AttnTcArgs& a, int rank, int pt, int64_t key_base, int k0, int kend) {
 #pragma unroll
@@ -211,17 +209,12 @@ struct Producer {
       const int idx = pt + t * kProducerThreads;
       const int key = idx / UPK, cu = idx % UPK;
       v[t] = make_uint4(0, 0, 0, 0);
-      if constexpr (kQ8) d[t] = 0u;
+      d[t] = 0u;
       if (idx < NUNITS && k0 + key < kend) {
         const int64_t row = key_base + k0 + key;
-        if constexpr (!kQ8) {
-          v[t] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.kv) + row * kRow + 256 * rank +
-                                                      cu * 8));
-        } else {
-          const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + kRopeHalf * rank + (cu - 16) * 16;
-          v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
-          d[t] = __ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row);
-        }
+        const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + kRopeHalf * rank + (cu - 16) * 16;
+        v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
+        d[t] = __ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row);
       }
     }
   }
@@ -232,23 +225,19 @@ struct Producer {
       const int idx = pt + t * kProducerThreads;
       const int key = idx / UPK, cu = idx % UPK;
       if (idx >= NUNITS) break;
-      if constexpr (!kQ8) {
-        st_unit(lat + (cu >> 3) * kChunk, key, cu & 7, bf16x8_to_f16x8(v[t]));
+      const int u = (cu & 3) * 2;
+      uint4 lo, hi;
+      const uint32_t d2 = d[t] | (d[t] << 16);
+      i8x4_to_f16x4(v[t].x, d2, lo.x, lo.y);
+      i8x4_to_f16x4(v[t].y, d2, lo.z, lo.w);
+      i8x4_to_f16x4(v[t].z, d2, hi.x, hi.y);
+      i8x4_to_f16x4(v[t].w, d2, hi.z, hi.w);
+      if (cu < 16) {
+        st_unit(lat + (cu >> 2) * kChunk, key, u, lo);
+        st_unit(lat + (cu >> 2) * kChunk, key, u + 1, hi);
       } else {
-        const int u = (cu & 3) * 2;
-        uint4 lo, hi;
-        const uint32_t d2 = d[t] | (d[t] << 16);
-        i8x4_to_f16x4(v[t].x, d2, lo.x, lo.y);
-        i8x4_to_f16x4(v[t].y, d2, lo.z, lo.w);
-        i8x4_to_f16x4(v[t].z, d2, hi.x, hi.y);
-        i8x4_to_f16x4(v[t].w, d2, hi.z, hi.w);
-        if (cu < 16) {
-          st_unit(lat + (cu >> 2) * kChunk, key, u, lo);
-          st_unit(lat + (cu >> 2) * kChunk, key, u + 1, hi);
-        } else {
-          st_unit64(rope, key, u, lo);
-          st_unit64(rope, key, u + 1, hi);
-        }
+        st_unit64(rope, key, u, lo);
+        st_unit64(rope, key, u + 1, hi);
       }
     }
   }
@@ -473,14 +462,12 @@ MLA_DEVINL void prefetch_q8_tile(const AttnTcArgs& a, const TileCursor<true>& c,
   }
 }
 
-// kRope: this producer writes the CTA's RoPE ring (q8_0 cache).  With a bf16
-// cache the RoPE tiles come by TMA, issued when `tma_rope` is set.
-// Tile u counts this cluster's tiles across items.
-template <bool kQ8, bool kRope>
-MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Bars& B, uint8_t* sLat,
-                             uint8_t* sRope, int rank, bool tma_rope, int pt, int first, int stride) {
-  using P = Producer<kQ8, kRope>;
-  const bool uses_rope = kRope || tma_rope;
+// The q8_0 decode's producer warps (thread pt of kProducerThreads): every
+// tile of this cluster's range into the latent and RoPE rings.  Tile u counts
+// this cluster's tiles across items.
+MLA_DEVINL void run_q8_producer(const AttnTcArgs& a, Bars& B, uint8_t* sLat, uint8_t* sRope, int rank, int pt,
+                                int first, int stride) {
+  using P = Q8Producer;
   TileCursor<true> cur;
   cur.init(a, first, stride, &B.ds);
   if (!cur.valid()) return;
@@ -493,7 +480,6 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
   }
   P x, y;
   uint32_t dmax = 0;                          // largest |scale| bit pattern (fp16 range check)
-  int64_t cur_row = cur.it.key_base + static_cast<int64_t>(cur.t) * kBK;
   x.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
   cur.next();
   // Tile u+1's loads are in flight while tile u is converted and stored.
@@ -503,7 +489,6 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
       ahead.next();
     }
     const bool more = cur.valid();
-    const int64_t nxt_row = more ? cur.it.key_base + static_cast<int64_t>(cur.t) * kBK : 0;
     if (more) {
       nxt.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
       cur.next();
@@ -511,24 +496,13 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
     const int ls = u % kLatStages, rs = u % kRopeStages;
     if (u >= kLatStages && !mbar_wait_bounded(&B.lat_empty[ls], ((u / kLatStages) - 1) & 1, a.wait_us, a.err))
       return false;
-    if (uses_rope && u >= kRopeStages &&
-        !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
+    if (u >= kRopeStages && !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
       return false;
-    if constexpr (!kQ8) {                     // bf16 RoPE keys by TMA, straight into the B-operand layout
-      if (tma_rope && pt == 0) {
-        mbar_arrive_expect_tx(&B.rope_full[rs], kRopeChunk);
-        tc::tma_load_3d(sRope + rs * kRopeChunk, tm_rope, &B.rope_full[rs], kLatent + kRopeHalf * rank,
-                        static_cast<int>(cur_row), 0);
-      }
-    }
     now.store(sLat + ls * kLatStage, sRope + rs * kRopeChunk, pt);
-    if constexpr (kQ8) {
 #pragma unroll
-      for (int t = 0; t < P::NU; ++t) dmax = max(dmax, now.d[t] & 0x7FFFu);
-    }
+    for (int t = 0; t < P::NU; ++t) dmax = max(dmax, now.d[t] & 0x7FFFu);
     tc::fence_proxy_async();
     mbar_arrive(&B.lat_full[ls]);
-    cur_row = nxt_row;
     return more;
   };
   // One copy of the step's code (the loop is not unrolled): after each tile
@@ -539,7 +513,7 @@ MLA_DEVINL void run_producer(const CUtensorMap* tm_rope, const AttnTcArgs& a, Ba
     if (!step(u, x, y)) break;
     x = y;
   }
-  if (kQ8 && f16_scale_overflows(dmax)) record_error(a.err, MLA_ERR_RANGE);
+  if (f16_scale_overflows(dmax)) record_error(a.err, MLA_ERR_RANGE);
 }
 
 // ---------------------------------------------------------------------------
@@ -1206,7 +1180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(kQ8, kDecode))
       // (bf16 decode: the two converter warps after this one run the
       // epilogue warps' conversion loop.)
     } else {
-      run_producer<true, true>(&tm_rope, a, B, sLat, sRope, static_cast<int>(rank), false, pt, first, stride);
+      run_q8_producer(a, B, sLat, sRope, static_cast<int>(rank), pt, first, stride);
     }
   } else {
     // ============================== MMA issue ==================================
