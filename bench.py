@@ -539,7 +539,11 @@ def run_ours(args, torch, dist, rank, world):
             if ":" in name:
                 sec = measure_variant(args, torch, name, flush, pk, pk_kind, world)
             else:
-                sec, _, _ = measure(args, torch, name, flush, pk, pk_kind, world)
+                sec, (swl, sx), _ = measure(args, torch, name, flush, pk, pk_kind, world)
+                if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                    # a smaller sample than the headline's; decode on 16 heads
+                    sec["cpu_baseline"] = cpu_baseline(swl, sx, sec["unit"], budget_s=args.cpu_budget / 4,
+                                                       n_heads=16 if swl.kind == "decode" else None)
             if mla.mla_get_device_error() != 0:
                 raise RuntimeError(f"device error during the {name} bench")
             out["secondary"][name] = sec
@@ -658,10 +662,11 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_sample(wl: W.Workload, x, rows: int):
+def oracle_sample(wl: W.Workload, x, rows: int, n_heads=None):
     """Run the oracle (un-absorbed definition) on the first `rows` query rows
     (prefill), sequences (decode) or new tokens (append); returns (seconds,
-    units done)."""
+    units done).  Decode with `n_heads`: only heads [0, n_heads), the seconds
+    scaled by n_head / n_heads (the oracle's work is proportional to heads)."""
     from oracle import mla_oracle as O
     t0 = time.perf_counter()
     if wl.kind == "append":
@@ -681,23 +686,27 @@ def oracle_sample(wl: W.Workload, x, rows: int):
         units = pairs * wl.n_head * FLOP_PER_PAIR_HEAD
     else:
         seqs = list(range(rows))
+        heads = None if n_heads is None else list(range(n_heads))
         O.decode_unabsorbed(x.q_nope, x.q_pe, x.c_kv, x.k_pe, x.wk_b, x.wv_b, x.seq_start, x.seq_len, wl.scale,
-                            seqs=seqs)
+                            heads=heads, seqs=seqs)
         row = 576 * 2 if wl.cache == "bf16" else 612
         units = int(x.seq_len[seqs].astype(np.int64).sum()) * row + len(seqs) * wl.n_head * (576 + 512) * 2
+        if n_heads is not None:
+            return (time.perf_counter() - t0) * wl.n_head / n_heads, units
     return time.perf_counter() - t0, units
 
 
-def cpu_baseline(wl, x, unit, budget_s=20.0):
+def cpu_baseline(wl, x, unit, budget_s=20.0, n_heads=None):
     rows = 4 if wl.kind != "decode" else 1
     cap = wl.B if wl.kind == "decode" else wl.T
-    sec, units = oracle_sample(wl, x, rows)
+    sec, units = oracle_sample(wl, x, rows, n_heads)
     # grow the sample toward the time budget, then report the largest
     while sec < budget_s / 4 and rows < cap:
         rows = min(rows * 4, cap)
-        sec, units = oracle_sample(wl, x, rows)
+        sec, units = oracle_sample(wl, x, rows, n_heads)
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    what = {"prefill": f"last {rows} query rows (all heads)", "decode": f"first {rows} sequences",
+    heads = "all heads" if n_heads is None else f"heads 0-{n_heads - 1} of {wl.n_head}, time scaled to all"
+    what = {"prefill": f"last {rows} query rows (all heads)", "decode": f"first {rows} sequences ({heads})",
             "append": f"first {rows} new tokens (rows + q8_0)"}[wl.kind]
     return {"value": units / sec / scale, "unit": unit, "cores": blas_threads(), "kind": "oracle",
             "sample": f"{what} of {wl.name}, un-absorbed numpy fp64 oracle, {sec:.2f} s"}
