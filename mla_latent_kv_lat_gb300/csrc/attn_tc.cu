@@ -130,8 +130,8 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units: P stays <= 256 in fp
 // warp during setup (a lane per sequence, so the sequence table costs two
 // round trips however many roles walk it), and read by every role.
 struct DecodeStart {
-  int64_t lo, hi;   // the cluster's tile range [lo, hi) in the run of all sequences' tiles
-  int64_t S;        // first tile of sequence b
+  int64_t lo, hi;   // the cluster's range [lo, hi) in the run of all sequences' costs
+  int64_t S;        // where sequence b's costs start in that run
   int b;            // the first sequence that ends after lo (n_seq: none)
 };
 
@@ -283,10 +283,12 @@ MLA_DEVINL Item prefill_item(const AttnTcArgs& a, int idx) {
 template <bool kDecode>
 struct ItemIter;
 
-// Whole warp.  Invalid sequences count 0 tiles (they are skipped).
+// Whole warp.  Invalid sequences cost nothing (they are skipped).
 MLA_DEVINL DecodeStart decode_start(const AttnTcArgs& a, int c, int g, int lane) {
   auto tiles = [&](int q) -> int64_t {
-    return q < a.n_seq ? decode_seq_tiles(decode_valid_len(a.seq_start, a.seq_len, q, a.max_len, a.n_rows)) : 0;
+    return q < a.n_seq ? decode_seq_cost(decode_valid_len(a.seq_start, a.seq_len, q, a.max_len, a.n_rows),
+                                         a.piece_cost)
+                       : 0;
   };
   int64_t T = 0;
   for (int q0 = 0; q0 < a.n_seq; q0 += 32) T += tiles(q0 + lane);
@@ -343,7 +345,7 @@ struct ItemIter<true> {
   const AttnTcArgs* a;
   int c;
   int b;                       // next sequence
-  int64_t lo, hi, S;           // cluster tile range, first tile of sequence b
+  int64_t lo, hi, S;           // cluster range, start of sequence b (in cost units)
   MLA_DEVINL void init(const AttnTcArgs& args, int cluster, int, const DecodeStart* ds) {
     a = &args; c = cluster;
     lo = ds->lo; hi = ds->hi; S = ds->S; b = ds->b;
@@ -351,14 +353,14 @@ struct ItemIter<true> {
   MLA_DEVINL bool next(Item& it) {
     while (b < a->n_seq && S < hi) {
       const int32_t len = decode_valid_len(a->seq_start, a->seq_len, b, a->max_len, a->n_rows);   // 0: skipped
-      const int64_t tb = decode_seq_tiles(len);
-      const int64_t p_lo = max(lo, S), p_hi = min(hi, S + tb);
+      const int64_t cost = decode_seq_cost(len, a->piece_cost);
+      const int64_t r0 = S + (len > 0 ? a->piece_cost : 0);   // where the sequence's tiles start
+      const int64_t p_lo = max(lo, r0), p_hi = min(hi, S + cost);
       const int bb = b;
-      const int64_t s0 = S;
-      S += tb;
+      S += cost;
       ++b;
       if (p_lo >= p_hi) continue;
-      const int64_t k0 = (p_lo - s0) * kBK;          // first key of the piece in its sequence
+      const int64_t k0 = (p_lo - r0) * kBK;          // first key of the piece in its sequence
       it.key_base = a->seq_start[bb] + k0;
       it.kend = static_cast<int>(min(static_cast<int64_t>(len) - k0, (p_hi - p_lo) * kBK));
       it.nvalid = a->n_head;

@@ -7,14 +7,21 @@
 
 namespace mla {
 
-// Split-KV decode, evenly over G clusters: the 64-key tiles of all sequences,
-// in sequence order, form one run of T tiles, and cluster c takes tiles
-// [c*T/G, (c+1)*T/G).  Where a cluster's range meets a sequence is a piece; it
-// produces one partial result, in slot b + c (pieces are ordered by sequence,
-// then cluster, and each starts at a sequence or cluster boundary).  Every
-// cluster does the same number of tiles (to one), whatever the lengths.
+// Split-KV decode, evenly over G clusters by cost.  A valid sequence of len
+// rows costs its 64-key tiles plus `piece_cost` more, the start of a piece
+// (its queries' load, the previous piece's output, the pipeline's refill)
+// counted in tiles; in sequence order these costs form one run of T units,
+// sequence b's start-up units first and then its tiles, and cluster c takes
+// units [c*T/G, (c+1)*T/G).  Where a cluster's range meets a sequence's tiles
+// is a piece; it produces one partial result, in slot b + c (pieces are
+// ordered by sequence, then cluster, and each starts at a sequence or cluster
+// boundary).  Every cluster does the same cost (to one unit): a cluster whose
+// range holds more pieces gets fewer tiles.
 constexpr int kDecodeTile = 64;
 MLA_DEVINL int64_t decode_seq_tiles(int32_t len) { return (static_cast<int64_t>(len) + kDecodeTile - 1) / kDecodeTile; }
+MLA_DEVINL int64_t decode_seq_cost(int32_t len, int piece_cost) {
+  return len > 0 ? decode_seq_tiles(len) + piece_cost : 0;
+}
 MLA_DEVINL int64_t decode_cluster_lo(int64_t T, int G, int c) { return T * c / G; }
 // Sequence b's length if its rows [seq_start, seq_start + len) are a valid
 // request (1 <= len <= max_len, inside the n_rows rows of the cache), else 0:
@@ -35,6 +42,7 @@ struct CombineArgs {
   int64_t n_rows;
   int* err;
   int B, n_head, n_clusters, max_len;
+  int piece_cost;           // the attention kernel's (see decode_seq_cost)
 };
 
 // C[t][h][n] = sum_k A[t][h][k] * W[h][k][n]  (absorb: bf16 A, K=128, N=512,
@@ -71,6 +79,7 @@ struct AttnTcArgs {
   const int32_t* seq_len;
   int n_seq;                // B
   int max_len;              // longest valid sequence (longer ones are skipped)
+  int piece_cost;           // start-up cost of a piece in tiles (see decode_seq_cost)
   float* ws_o;              // fp32 [B + G - 1][H][512] partial o_lat per piece, normalised by its own sum
   float* ws_ml;             // fp32 [B + G - 1][H][2]   running max (log2 units) and sum
   int* err;

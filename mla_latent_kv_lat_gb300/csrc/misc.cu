@@ -74,11 +74,13 @@ constexpr int kCombHeads = 8;
 __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // This sequence's tiles [Sb, Eb) in the run of all sequences' tiles.
+  // This sequence's costs [Sb, Eb) in the run of all sequences' costs; its
+  // tiles are [Sb + piece_cost, Eb).
   __shared__ long long red[2][kCombHeads];
   long long tb = 0, tt = 0;
   for (int q = threadIdx.x; q < c.B; q += blockDim.x) {
-    const long long t = decode_seq_tiles(decode_valid_len(c.seq_start, c.seq_len, q, c.max_len, c.n_rows));
+    const long long t = decode_seq_cost(decode_valid_len(c.seq_start, c.seq_len, q, c.max_len, c.n_rows),
+                                        c.piece_cost);
     tt += t;
     if (q < b) tb += t;
   }
@@ -100,7 +102,8 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
     if (threadIdx.x == 0 && blockIdx.y == 0) record_error(c.err, MLA_ERR_INVALID_ARG);
     return;
   }
-  const int64_t Eb = Sb + decode_seq_tiles(len_b);
+  const int64_t Eb = Sb + decode_seq_cost(len_b, c.piece_cost);
+  const int64_t Rb = Sb + c.piece_cost;                // the first of its tiles
   const int G = c.n_clusters;
   // The clusters' range starts lo(x) = T x / G, x = 0..G, once per block (a
   // 64-bit division each: computed on the fly they made this kernel
@@ -109,10 +112,11 @@ __global__ void __launch_bounds__(32 * kCombHeads) combine_kernel(CombineArgs c)
   for (int x = threadIdx.x; x <= G; x += blockDim.x) s_lo[x] = decode_cluster_lo(T, G, x);
   __syncthreads();
   auto lo = [&](int x) { return s_lo[x]; };
-  // The first cluster whose range meets [Sb, Eb): ranges are [lo(c), lo(c+1)).
-  int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Sb * G / max(T, static_cast<int64_t>(1))));
-  while (c0 > 0 && lo(c0) > Sb) --c0;
-  while (c0 + 1 < G && lo(c0 + 1) <= Sb) ++c0;
+  // The first cluster whose range meets the tiles [Rb, Eb): ranges are
+  // [lo(c), lo(c+1)); every later one that meets them has lo(c) < Eb.
+  int c0 = static_cast<int>(min(static_cast<int64_t>(G - 1), Rb * G / max(T, static_cast<int64_t>(1))));
+  while (c0 > 0 && lo(c0) > Rb) --c0;
+  while (c0 + 1 < G && lo(c0 + 1) <= Rb) ++c0;
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the attention kernel's partials are complete
   const int h = blockIdx.y * kCombHeads + warp;
   if (h >= c.n_head) return;
