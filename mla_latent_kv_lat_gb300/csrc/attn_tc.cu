@@ -193,7 +193,12 @@ MLA_DEVINL uint4 bf16x8_to_f16x8(uint4 v) {
 // ---------------------------------------------------------------------------
 // q8_0 decode producer: one 64-key tile of this CTA's cache part, the 256
 // latent dims (16 units of 16 codes per key) plus this CTA's 32 RoPE dims (2
-// units), dequantised to fp16 (fp16 scale x int8 code).
+// units), dequantised to fp16 (fp16 scale x int8 code).  The 1152 units of a
+// tile are dealt out so that each warp load instruction reads 4 keys x 8
+// latent units: 128 contiguous code bytes of each key and 4 scales from each
+// of 4 block rows, 8 cache lines in all.  (Dealt out key by key, 18 units at a
+// time, an instruction touched ~19 lines, and the loads' L1 wavefronts made
+// the q8_0 decode 11% slower.)
 // ---------------------------------------------------------------------------
 struct Q8Producer {
   static constexpr int UPK = 16 + 2;
@@ -203,42 +208,79 @@ struct Q8Producer {
   uint32_t d[NU];   // raw fp16 scale bits: converted at store time, so no
                     // instruction waits on the load before then
 
-  MLA_DEVINL void load(const AttnTcArgs& a, int rank, int pt, int64_t key_base, int k0, int kend) {
+  // Unit idx of a tile -> (key, code unit cu): idx < 1024 are the latent units,
+  // 32 consecutive ones = units [8g, 8g + 8) of 4 consecutive keys; then the
+  // RoPE units, two per key.
+  MLA_DEVINL static void unit_of(int idx, int& key, int& cu) {
+    static_assert(kBK == 64 && UPK == 18, "unit_of deals 64-key tiles of 18 units");
+    if (idx < kBK * 16) {
+      key = (idx >> 3) & (kBK - 1);
+      cu = ((idx >> 9) << 3) + (idx & 7);
+    } else {
+      key = (idx - kBK * 16) >> 1;
+      cu = 16 + (idx & 1);
+    }
+  }
+
+  // Per-thread constants of the thread's units, the same for every tile
+  // (computed once: the address arithmetic per unit and tile cost 4% of the
+  // q8_0 decode): so = byte offset of the unit's low 16 bytes in its stage
+  // (latent or RoPE; the high 16 bytes sit at so ^ 16), lc = key (bits 0-5),
+  // scale block (bits 6-10) and code offset from the tile's first row (bits
+  // 16-31, < 64 x 576).  pt's range lets the compiler resolve which rounds
+  // hold latent units, which RoPE units and which none (3.5%).
+  struct Plan {
+    uint32_t so[NU], lc[NU];
+  };
+  MLA_DEVINL static void plan(Plan& p, int rank, int pt) {
+    __builtin_assume(pt >= 0 && pt < kProducerThreads);
 #pragma unroll
     for (int t = 0; t < NU; ++t) {
       const int idx = pt + t * kProducerThreads;
-      const int key = idx / UPK, cu = idx % UPK;
+      int key, cu;
+      unit_of(idx, key, cu);
+      const int u = (cu & 3) * 2;
+      const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + kRopeHalf * rank + (cu - 16) * 16;
+      p.so[t] = cu < 16 ? (cu >> 2) * kChunk + key * 128 + ((u ^ (key & 7)) << 4)   // st_unit's layout
+                        : key * 64 + ((u ^ ((key >> 1) & 3)) << 4);                 // st_unit64's
+      p.lc[t] = static_cast<uint32_t>(key) | (static_cast<uint32_t>(dim >> 5) << 6) |
+                (static_cast<uint32_t>(key * kRow + dim) << 16);
+    }
+  }
+
+  MLA_DEVINL void load(const AttnTcArgs& a, const Plan& p, int pt, int64_t key_base, int k0, int kend) {
+    __builtin_assume(pt >= 0 && pt < kProducerThreads);
+    const int64_t r0 = key_base + k0;
+    const int8_t* codes = a.kv_q + r0 * kRow;
+    const uint16_t* scales = a.kv_d + r0;
+#pragma unroll
+    for (int t = 0; t < NU; ++t) {
+      const int idx = pt + t * kProducerThreads;
       v[t] = make_uint4(0, 0, 0, 0);
       d[t] = 0u;
+      const int key = static_cast<int>(p.lc[t] & 63u);
       if (idx < NUNITS && k0 + key < kend) {
-        const int64_t row = key_base + k0 + key;
-        const int dim = cu < 16 ? 256 * rank + cu * 16 : kLatent + kRopeHalf * rank + (cu - 16) * 16;
-        v[t] = __ldg(reinterpret_cast<const uint4*>(a.kv_q + row * kRow + dim));
-        d[t] = __ldg(a.kv_d + static_cast<int64_t>(dim >> 5) * a.ld_d + row);
+        v[t] = __ldg(reinterpret_cast<const uint4*>(codes + (p.lc[t] >> 16)));
+        d[t] = __ldg(scales + static_cast<int64_t>((p.lc[t] >> 6) & 31u) * a.ld_d + key);
       }
     }
   }
 
-  MLA_DEVINL void store(uint8_t* lat, uint8_t* rope, int pt) const {
+  MLA_DEVINL void store(const Plan& p, uint8_t* lat, uint8_t* rope, int pt) const {
+    __builtin_assume(pt >= 0 && pt < kProducerThreads);
 #pragma unroll
     for (int t = 0; t < NU; ++t) {
       const int idx = pt + t * kProducerThreads;
-      const int key = idx / UPK, cu = idx % UPK;
       if (idx >= NUNITS) break;
-      const int u = (cu & 3) * 2;
       uint4 lo, hi;
       const uint32_t d2 = d[t] | (d[t] << 16);
       i8x4_to_f16x4(v[t].x, d2, lo.x, lo.y);
       i8x4_to_f16x4(v[t].y, d2, lo.z, lo.w);
       i8x4_to_f16x4(v[t].z, d2, hi.x, hi.y);
       i8x4_to_f16x4(v[t].w, d2, hi.z, hi.w);
-      if (cu < 16) {
-        st_unit(lat + (cu >> 2) * kChunk, key, u, lo);
-        st_unit(lat + (cu >> 2) * kChunk, key, u + 1, hi);
-      } else {
-        st_unit64(rope, key, u, lo);
-        st_unit64(rope, key, u + 1, hi);
-      }
+      uint8_t* base = idx < kBK * 16 ? lat : rope;
+      *reinterpret_cast<uint4*>(base + p.so[t]) = lo;
+      *reinterpret_cast<uint4*>(base + (p.so[t] ^ 16u)) = hi;
     }
   }
 };
@@ -449,7 +491,7 @@ MLA_DEVINL void prefetch_rows_l2(const AttnTcArgs& a, int64_t row0, int64_t nrow
 // producers' loads.
 constexpr int kPrefetchTiles = 8;
 
-// q8_0 tiles ahead, by one warp (lane = pt < 32): the codes as one bulk L2
+// q8_0 tiles ahead, by one warp (`lane` its lane): the codes as one bulk L2
 // prefetch, and the scales of the tile's rows in each of the 18 scale blocks
 // (lanes 0..17: the first and the last cache line of the block's run).
 MLA_DEVINL void prefetch_q8_tile(const AttnTcArgs& a, const TileCursor<true>& c, int lane) {
@@ -473,26 +515,30 @@ MLA_DEVINL void run_q8_producer(const AttnTcArgs& a, Bars& B, uint8_t* sLat, uin
   TileCursor<true> cur;
   cur.init(a, first, stride, &B.ds);
   if (!cur.valid()) return;
-  // One thread keeps the rows of the tiles kPrefetchTiles ahead on their way into L2.
+  // One warp keeps the rows of the tiles kPrefetchTiles ahead on their way into
+  // L2: the last one, which has a unit fewer per tile than the first.
   TileCursor<true> ahead = cur;
-  const bool pf = pt < 32 && rank == 0;
+  const bool pf = pt >= kProducerThreads - 32 && rank == 0;
+  const int pl = pt - (kProducerThreads - 32);
   for (int d = 0; d < kPrefetchTiles && ahead.valid(); ++d) {
-    if (pf) prefetch_q8_tile(a, ahead, pt);
+    if (pf) prefetch_q8_tile(a, ahead, pl);
     ahead.next();
   }
+  P::Plan plan;
+  P::plan(plan, rank, pt);
   P x, y;
   uint32_t dmax = 0;                          // largest |scale| bit pattern (fp16 range check)
-  x.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
+  x.load(a, plan, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
   cur.next();
   // Tile u+1's loads are in flight while tile u is converted and stored.
   auto step = [&](int u, P& now, P& nxt) -> bool {
     if (ahead.valid()) {
-      if (pf) prefetch_q8_tile(a, ahead, pt);
+      if (pf) prefetch_q8_tile(a, ahead, pl);
       ahead.next();
     }
     const bool more = cur.valid();
     if (more) {
-      nxt.load(a, rank, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
+      nxt.load(a, plan, pt, cur.it.key_base, cur.t * kBK, cur.it.kend);
       cur.next();
     }
     const int ls = u % kLatStages, rs = u % kRopeStages;
@@ -500,7 +546,7 @@ MLA_DEVINL void run_q8_producer(const AttnTcArgs& a, Bars& B, uint8_t* sLat, uin
       return false;
     if (u >= kRopeStages && !mbar_wait_bounded(&B.rope_empty[rs], ((u / kRopeStages) - 1) & 1, a.wait_us, a.err))
       return false;
-    now.store(sLat + ls * kLatStage, sRope + rs * kRopeChunk, pt);
+    now.store(plan, sLat + ls * kLatStage, sRope + rs * kRopeChunk, pt);
 #pragma unroll
     for (int t = 0; t < P::NU; ++t) dmax = max(dmax, now.d[t] & 0x7FFFu);
     tc::fence_proxy_async();
